@@ -1,0 +1,498 @@
+"""Benchmark of the fine-grained FP8 hot path on B300.
+
+One step = one training pass of a linear layer (tokens 4096, K_in 7168,
+N_out 18432) through every row of the path:
+    quant 1x128 (X) -> quant 128x128 (W, with transposed copy) -> Fprop GEMM
+    quant 1x128 (dY) -> Dgrad GEMM
+    quant 128x1 (X), quant 128x1 (dY) -> Wgrad GEMM (FP32 out)
+`value` = the three GEMMs' FLOPs (3 x 2*M*N*K) / device time of the whole step,
+in TFLOPS, with inputs resident in HBM.  Per-kernel CUDA-event timings give the
+roofline of the dominant kernel and of every other launch.  `e2e` repeats the
+step through the same entry points from pinned host buffers, copies included.
+Extras (not part of `value`): the grouped MoE up-projection and the quantizer
+bandwidth sweep.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fp8bs|reference]
+
+Under torchrun each rank runs an independent replica (no data-path collective);
+the barrier / max-over-ranks timing uses torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+TOKENS, HIDDEN, FFN = wl.TOKENS, wl.HIDDEN, wl.FFN
+GEMM_FLOPS = 2.0 * TOKENS * HIDDEN * FFN          # each of Fprop, Dgrad, Wgrad
+METRIC = "block-scaled FP8 GEMM TFLOPS (% of B300 FP8 peak); quantizer GB/s (% of HBM)"
+WORKLOAD = ("linear-layer training step: quant 1x128/128x1/128x128 + Fprop, Dgrad, Wgrad "
+            f"block-scaled FP8 GEMMs, tokens={TOKENS}, K={HIDDEN}, N={FFN}")
+
+# Algorithmic bytes per element of the quantizers (read input, write codes, write scales).
+def quant_bytes(elems: int, in_bytes: int, transposed_copy: bool = False, block=False) -> float:
+    scale = 4.0 / (128 * 128) if block else 4.0 / 128
+    return elems * (in_bytes + 1 + (1 if transposed_copy else 0) + scale)
+
+
+# DRAM traffic per launch measured by ncu (dram__bytes_read.sum + write.sum), with
+# the sha256 of the kernel source it was measured on; ignored once the source changes.
+NCU_TRAFFIC = {}
+
+
+def _src_hash(name: str) -> str:
+    p = os.path.join(ROOT, "fp8_fine_grained_15_b300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    hbm, bf16, src = 6400.0, 1800.0, "fallback"
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        hbm, bf16, src = float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    # FP8 dense = 2 x BF16 dense (nominal ratio 4.5 / 2.25 PFLOP/s).
+    return {"hbm_gbs": hbm, "fp8_tflops": 2.0 * bf16, "source": src}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- the step
+
+class LayerStep:
+    """Device buffers and the launch sequence of one layer training step."""
+
+    KERNELS = ["quant_1x128_X", "quant_128x128_W", "gemm_fprop", "quant_1x128_dY",
+               "gemm_dgrad", "quant_128x1_X", "quant_128x1_dY", "gemm_wgrad"]
+
+    def __init__(self, x, w, dy, dev):
+        import fp8_fine_grained_15_b300 as fb
+        self.fb = fb
+        T, K = x.shape
+        N = w.shape[1]
+        e = lambda *s, dt=torch.uint8: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+        self.x, self.w, self.dy = x, w, dy
+        self.Xq, self.Sx = e(T, K), e(K // 128, T, dt=torch.float32)
+        self.Wq, self.WqT, self.Sw = e(K, N), e(N, K), e(K // 128, N // 128, dt=torch.float32)
+        self.dYq, self.Sdy = e(T, N), e(N // 128, T, dt=torch.float32)
+        self.XqT, self.SxT = e(K, T), e(T // 128, K, dt=torch.float32)
+        self.dYqT, self.SdyT = e(N, T), e(T // 128, N, dt=torch.float32)
+        self.Y = e(T, N, dt=torch.bfloat16)
+        self.dX = e(T, K, dt=torch.bfloat16)
+        self.dW = e(K, N, dt=torch.float32)
+        self.T, self.K, self.N = T, K, N
+
+    def launches(self):
+        fb = self.fb
+        return [
+            lambda s: fb.fp8bs_quant_act_1x128(self.x, self.Xq, self.Sx, s),
+            lambda s: fb.fp8bs_quant_w_128x128(self.w, self.Wq, self.WqT, self.Sw, s),
+            lambda s: fb.fp8bs_gemm(self.Xq, self.Sx, self.WqT, self.Sw, fb.FP8BS_SB_BLOCK_KN,
+                                    self.Y, s),
+            lambda s: fb.fp8bs_quant_act_1x128(self.dy, self.dYq, self.Sdy, s),
+            lambda s: fb.fp8bs_gemm(self.dYq, self.Sdy, self.Wq, self.Sw, fb.FP8BS_SB_BLOCK_NK,
+                                    self.dX, s),
+            lambda s: fb.fp8bs_quant_act_128x1(self.x, self.XqT, self.SxT, s),
+            lambda s: fb.fp8bs_quant_act_128x1(self.dy, self.dYqT, self.SdyT, s),
+            lambda s: fb.fp8bs_gemm(self.XqT, self.SxT, self.dYqT, self.SdyT, fb.FP8BS_SB_PERCOL,
+                                    self.dW, s),
+        ]
+
+    def work(self):
+        """(kind, algorithmic amount) per launch: bytes for quantizers, FLOPs for GEMMs."""
+        T, K, N = self.T, self.K, self.N
+        g = 2.0 * T * K * N
+        return [("hbm", quant_bytes(T * K, 2)), ("hbm", quant_bytes(K * N, 2, True, True)),
+                ("tensor", g), ("hbm", quant_bytes(T * N, 2)), ("tensor", g),
+                ("hbm", quant_bytes(T * K, 2)), ("hbm", quant_bytes(T * N, 2)), ("tensor", g)]
+
+
+def _barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(v: float, dist_on: bool) -> float:
+    if not dist_on:
+        return v
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.distributed.get_backend() == "nccl" else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_fp8bs(args, rank, world, dist_on):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks = _peaks()
+    # Inputs: seeded host generation (identical recipe to the parity tests),
+    # one independent replica per rank (seeds offset by rank).
+    x_h = wl.layer_activations(seed=0 + 10 * rank)
+    w_h = wl.layer_weight(seed=1 + 10 * rank)
+    dy_h = wl.layer_grad_output(seed=2 + 10 * rank)
+    x, w, dy = x_h.to(dev), w_h.to(dev), dy_h.to(dev)
+    step = LayerStep(x, w, dy, dev)
+    stream = torch.cuda.current_stream(dev)
+    fns = step.launches()
+    nk = len(fns)
+
+    for _ in range(args.warmup):
+        for f in fns:
+            f(stream)
+    torch.cuda.synchronize(dev)
+    st = step.fb.fp8bs_sync_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {step.fb.status_string(st)}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    _barrier(dist_on)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            for i, f in enumerate(fns):
+                f(stream)
+                ev[k][i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    _barrier(dist_on)
+    if step.fb.fp8bs_sync_status(stream) != 0:
+        raise RuntimeError("device error during the timed region")
+    total_ms = sum(ev[k][0].elapsed_time(ev[k][nk]) for k in range(args.steps))
+    per_kernel_ms = [statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1])
+                                     for k in range(args.steps)) for i in range(nk)]
+    ms_per_step = _max_over_ranks(total_ms / args.steps, dist_on)
+    value = world * 3 * GEMM_FLOPS / (ms_per_step * 1e-3) / 1e12
+
+    kernels = {}
+    for name, ms, (kind, amount) in zip(LayerStep.KERNELS, per_kernel_ms, step.work()):
+        if kind == "tensor":
+            ach = amount / (ms * 1e-3) / 1e12
+            kernels[name] = {"ms": round(ms, 4), "TFLOP/s": round(ach, 1),
+                             "frac_fp8_peak": round(ach / peaks["fp8_tflops"], 4)}
+        else:
+            ach = amount / (ms * 1e-3) / 1e9
+            kernels[name] = {"ms": round(ms, 4), "GB/s": round(ach, 1),
+                             "frac_hbm": round(ach / peaks["hbm_gbs"], 4)}
+    dom = max(range(nk), key=lambda i: per_kernel_ms[i])
+    dom_name = LayerStep.KERNELS[dom]
+    kind, amount = step.work()[dom]
+    if kind == "tensor":
+        ach = amount / (per_kernel_ms[dom] * 1e-3) / 1e12
+        peak, unit = peaks["fp8_tflops"], "TFLOP/s"
+    else:
+        ach = amount / (per_kernel_ms[dom] * 1e-3) / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    traffic = None
+    rec = NCU_TRAFFIC.get(dom_name)
+    if rec and rec["src"] == _src_hash(rec["file"]):
+        traffic = rec["bytes"]
+    roofline = {"bound": kind, "kernel": dom_name, "achieved": round(ach, 2),
+                "peak": round(peak, 1), "unit": unit, "frac": round(ach / peak, 4),
+                "traffic": traffic,
+                "peak_source": f"{peaks['source']}: FP8 = 2 x bf16 burst; HBM copy"}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(step, x_h, w_h, dy_h, dev, stream, args, dist_on, world)
+    extras = None if args.no_extras else run_extras(dev, stream, peaks)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(seconds_hint=args.cpu_seconds)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded numpy: N(0,1) activations with 0.1% x100 outliers, "
+                "N(0,0.02) weights, N(0,1e-3) output grads; bf16)",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS, "K": HIDDEN, "N": FFN,
+                   "l2": "inputs larger than L2 (474 MB of bf16 inputs per step)",
+                   "parallelism": f"replicas x{world} (no data-path collective)"},
+        "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": nk * args.steps, "clocks": clk.summary(), "extras": extras,
+    }
+    return result
+
+
+def run_e2e(step, x_h, w_h, dy_h, dev, stream, args, dist_on, world):
+    """The same step from pinned host buffers: H2D of X, W, dY, the eight
+    library calls, D2H of Y, dX, dW, all inside the timed region."""
+    xp, wp, dyp = x_h.pin_memory(), w_h.pin_memory(), dy_h.pin_memory()
+    Yh = torch.empty(step.Y.shape, dtype=step.Y.dtype).pin_memory()
+    dXh = torch.empty(step.dX.shape, dtype=step.dX.dtype).pin_memory()
+    dWh = torch.empty(step.dW.shape, dtype=step.dW.dtype).pin_memory()
+    fns = step.launches()
+
+    def one():
+        step.x.copy_(xp, non_blocking=True)
+        step.w.copy_(wp, non_blocking=True)
+        step.dy.copy_(dyp, non_blocking=True)
+        for f in fns:
+            f(stream)
+        Yh.copy_(step.Y, non_blocking=True)
+        dXh.copy_(step.dX, non_blocking=True)
+        dWh.copy_(step.dW, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize(dev)
+    n = max(2, min(args.steps, 5))
+    _barrier(dist_on)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(dist_on)
+    ms = _max_over_ranks(s.elapsed_time(e) / n, dist_on)
+    h2d = sum(t.numel() * t.element_size() for t in (xp, wp, dyp))
+    d2h = sum(t.numel() * t.element_size() for t in (Yh, dXh, dWh))
+    return {"value": round(world * 3 * GEMM_FLOPS / (ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_extras(dev, stream, peaks):
+    """Grouped MoE up-projection (32 experts, Zipf(1.1) routing of 16384 rows,
+    7168 -> 4096) and the quantizer bandwidth sweep, timed with CUDA events.
+    Inputs are drawn on the device with a seeded generator (timing only)."""
+    import fp8_fine_grained_15_b300 as fb
+    out = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+
+    def timeit(fn, reps=10, flush=None):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            if flush is not None:
+                flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(s.elapsed_time(e))
+        return statistics.median(ts), min(ts)
+
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > L2
+
+    # grouped GEMM
+    counts = wl.zipf_counts()
+    offsets = wl.padded_offsets(counts)
+    E, K, N = wl.EXPERTS, wl.HIDDEN, wl.EXPERT_N
+    M_cap = int(offsets[-1])
+    Aq = torch.randint(0, 0x7E, (M_cap, K), dtype=torch.uint8, device=dev, generator=gen)
+    sa = torch.rand((K // 128, M_cap), device=dev, generator=gen) * 1e-2
+    Bq = torch.randint(0, 0x7E, (E, N, K), dtype=torch.uint8, device=dev, generator=gen)
+    sb = torch.rand((E, K // 128, N // 128), device=dev, generator=gen) * 1e-3
+    C = torch.empty((M_cap, N), dtype=torch.bfloat16, device=dev)
+    off = torch.tensor(offsets.astype(np.int32), device=dev)
+    med, best = timeit(lambda: fb.fp8bs_grouped_gemm(off, Aq, sa, Bq, sb, fb.FP8BS_SB_BLOCK_KN,
+                                                     C, stream), flush=flush)
+    flops_real = 2.0 * int(counts.sum()) * K * N
+    flops_pad = 2.0 * M_cap * K * N
+    out["grouped_moe_up"] = {
+        "experts": E, "rows_routed": int(counts.sum()), "rows_padded": M_cap,
+        "ms_median": round(med, 4),
+        "TFLOP/s_unpadded": round(flops_real / (med * 1e-3) / 1e12, 1),
+        "TFLOP/s_padded": round(flops_pad / (med * 1e-3) / 1e12, 1),
+        "frac_fp8_peak_unpadded": round(flops_real / (med * 1e-3) / 1e12 / peaks["fp8_tflops"], 4)}
+    del Aq, Bq, C, sa, sb
+
+    # quantizer sweep
+    sweep = {}
+    for M in (1024, 8192, 65536):
+        x = torch.randn((M, wl.HIDDEN), device=dev, generator=gen).to(torch.bfloat16)
+        q = torch.empty((M, wl.HIDDEN), dtype=torch.uint8, device=dev)
+        s = torch.empty((wl.HIDDEN // 128, M), dtype=torch.float32, device=dev)
+        qT = torch.empty((wl.HIDDEN, M), dtype=torch.uint8, device=dev)
+        sT = torch.empty((M // 128, wl.HIDDEN), dtype=torch.float32, device=dev)
+        nbytes = quant_bytes(M * wl.HIDDEN, 2)
+        m1, _ = timeit(lambda: fb.fp8bs_quant_act_1x128(x, q, s, stream), flush=flush)
+        m2, _ = timeit(lambda: fb.fp8bs_quant_act_128x1(x, qT, sT, stream), flush=flush)
+        sweep[f"M{M}"] = {
+            "bytes": int(nbytes),
+            "1x128_us": round(m1 * 1e3, 2), "1x128_GB/s": round(nbytes / (m1 * 1e-3) / 1e9, 1),
+            "1x128_frac_hbm": round(nbytes / (m1 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "128x1_us": round(m2 * 1e3, 2), "128x1_GB/s": round(nbytes / (m2 * 1e-3) / 1e9, 1),
+            "128x1_frac_hbm": round(nbytes / (m2 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+        del x, q, s, qT, sT
+    wgt = torch.randn((wl.HIDDEN, wl.FFN), device=dev, generator=gen).to(torch.bfloat16)
+    wq = torch.empty((wl.HIDDEN, wl.FFN), dtype=torch.uint8, device=dev)
+    wqT = torch.empty((wl.FFN, wl.HIDDEN), dtype=torch.uint8, device=dev)
+    ws = torch.empty((wl.HIDDEN // 128, wl.FFN // 128), dtype=torch.float32, device=dev)
+    for name, qq, tt, tr in (("128x128", wq, None, False), ("128x128+T", wq, wqT, True)):
+        nbytes = quant_bytes(wl.HIDDEN * wl.FFN, 2, tr, True)
+        m, _ = timeit(lambda: fb.fp8bs_quant_w_128x128(wgt, qq, tt, ws, stream), flush=flush)
+        sweep[f"W_{name}"] = {"bytes": int(nbytes), "us": round(m * 1e3, 2),
+                              "GB/s": round(nbytes / (m * 1e-3) / 1e9, 1),
+                              "frac_hbm": round(nbytes / (m * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    out["quant_sweep"] = sweep
+    if fb.fp8bs_sync_status(stream) != 0:
+        raise RuntimeError("device error during extras")
+    return out
+
+
+# ------------------------------------------------------ CPU oracle baseline
+
+CPU_SAMPLE = {"tokens": 256, "K": HIDDEN, "N": 1536}
+
+
+def cpu_baseline(seconds_hint: float = 0.0):
+    """The oracle, as it stands (single-threaded C), on a bounded sample of the
+    layer step: the same eight operations on 256 tokens x 7168 x 1536."""
+    import oracle
+    from workloads import bf16_bits
+    T, K, N = CPU_SAMPLE["tokens"], CPU_SAMPLE["K"], CPU_SAMPLE["N"]
+    x = bf16_bits(wl.layer_activations(T, K))
+    w = bf16_bits(wl.layer_weight(K, N))
+    dy = bf16_bits(wl.layer_grad_output(T, N))
+    oracle.build()
+    t0 = time.perf_counter()
+    Xq, Sx = oracle.quant_act_1x128(x)
+    Wq, WqT, Sw = oracle.quant_w_128x128(w)
+    oracle.gemm(Xq, Sx, WqT, Sw, oracle.SB_BLOCK_KN)
+    dYq, Sdy = oracle.quant_act_1x128(dy)
+    oracle.gemm(dYq, Sdy, Wq, np.ascontiguousarray(Sw.T), oracle.SB_BLOCK_NK)
+    XqT, SxT = oracle.quant_act_128x1(x)
+    dYqT, SdyT = oracle.quant_act_128x1(dy)
+    oracle.gemm(XqT, SxT, dYqT, SdyT, oracle.SB_PERCOL)
+    dt = time.perf_counter() - t0
+    flops = 3 * 2.0 * T * K * N
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOPS", "cores": 1,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"full layer step (8 ops) on tokens={T}, K={K}, N={N}; "
+                      f"single-threaded C oracle, FP64 GEMM"}
+
+
+def run_reference(args, rank, world, dist_on):
+    """The reference arm: the CPU oracle, timed on the host, on a bounded
+    sample of the same workload, each step one sample."""
+    if rank != 0:
+        return None
+    for _ in range(max(0, min(args.warmup, 1))):
+        cpu_baseline()
+    vals, secs = [], []
+    for _ in range(args.steps):
+        r = cpu_baseline()
+        vals.append(r["value"])
+        secs.append(r["seconds"])
+    v = statistics.median(vals)
+    T, K, N = CPU_SAMPLE["tokens"], CPU_SAMPLE["K"], CPU_SAMPLE["N"]
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.median(secs) * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy, same recipe as the fp8bs arm)",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS, "K": HIDDEN, "N": FFN,
+                   "sample": f"tokens={T}, K={K}, N={N} per step"},
+        "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": 1, "kind": "oracle",
+                         "sample": f"layer step on tokens={T}, K={K}, N={N}"},
+        "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["fp8bs", "reference"], default="fp8bs")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=0.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "fp8bs":
+        ap.error("at least 3 warm-up steps")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist_on = world > 1
+    if dist_on:
+        backend = "nccl" if (torch.cuda.is_available() and args.impl == "fp8bs") else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group(backend)
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world, dist_on)
+    else:
+        res = run_fp8bs(args, rank, world, dist_on)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

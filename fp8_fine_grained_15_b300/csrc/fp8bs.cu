@@ -1,0 +1,388 @@
+// C ABI of the fp8bs library: host-side argument checks, TMA descriptor
+// encoding and kernel launches.  Declarations and the full contract are in
+// include/fp8bs.h.  Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fp8bs.h"
+#include "gemm_kernel.cuh"
+#include "quant_kernels.cuh"
+
+namespace fp8bs {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool init = false;
+  int num_sms = 0;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+fp8bs_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8BS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
+    d.init = true;
+  }
+  *out = d;
+  return FP8BS_OK;
+}
+
+fp8bs_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return FP8BS_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = g_encode;
+  return FP8BS_OK;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline size_t dtype_size(fp8bs_dtype t) { return t == FP8BS_F32 ? 4 : 2; }
+
+inline bool valid_dtype(fp8bs_dtype t) { return t == FP8BS_F32 || t == FP8BS_BF16; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+fp8bs_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
+// 2D u8 map over rows x inner bytes, box 128 x box_rows, 128-byte swizzle.
+fp8bs_status make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                         uint64_t row_stride, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  fp8bs_status st = encode_fn(&enc);
+  if (st != FP8BS_OK) return st;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_stride};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
+// 3D u8 map over [E][rows][inner], box 128 x box_rows x 1.
+fp8bs_status make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                         uint64_t E, uint64_t row_stride, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  fp8bs_status st = encode_fn(&enc);
+  if (st != FP8BS_OK) return st;
+  cuuint64_t dims[3] = {inner, rows, E};
+  cuuint64_t strides[2] = {row_stride, row_stride * rows};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
+// Shared checks of the dense and grouped GEMM (all on the host, before any launch).
+fp8bs_status check_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                        const float* sa, int64_t ldsa, const uint8_t* B, int64_t ldb,
+                        const float* sb, fp8bs_bscale sb_mode, int64_t ldsb, const void* C,
+                        fp8bs_dtype ct, int64_t ldc) {
+  if (M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if (!valid_dtype(ct)) return FP8BS_ERR_INVALID_ARG;
+  if (sb_mode != FP8BS_SB_BLOCK_NK && sb_mode != FP8BS_SB_BLOCK_KN && sb_mode != FP8BS_SB_PERCOL)
+    return FP8BS_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return FP8BS_OK;
+  if (K % kBK != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (sb_mode == FP8BS_SB_PERCOL ? (N % 16 != 0) : (N % 128 != 0)) return FP8BS_ERR_UNSUPPORTED;
+  if (M > INT_MAX - kBM || N > INT_MAX - kBN || K / kBK > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+  if (C == nullptr || ldc < N) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned(C, 16) || (ldc * static_cast<int64_t>(dtype_size(ct))) % 16 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  if (K == 0) return FP8BS_OK;
+  if (A == nullptr || B == nullptr || sa == nullptr || sb == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldsa < M) return FP8BS_ERR_INVALID_ARG;
+  if (sb_mode == FP8BS_SB_BLOCK_NK && ldsb < K / 128) return FP8BS_ERR_INVALID_ARG;
+  if (sb_mode == FP8BS_SB_BLOCK_KN && ldsb < N / 128) return FP8BS_ERR_INVALID_ARG;
+  if (sb_mode == FP8BS_SB_PERCOL && ldsb < N) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || lda % 16 != 0 || ldb % 16 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  if (!aligned(sa, 4) || !aligned(sb, 4)) return FP8BS_ERR_MISALIGNED;
+  if (sb_mode == FP8BS_SB_PERCOL && (!aligned(sb, 16) || ldsb % 4 != 0))
+    return FP8BS_ERR_MISALIGNED;
+  return FP8BS_OK;
+}
+
+template <bool kGrouped>
+fp8bs_status launch_gemm(GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                         int sb_kind, fp8bs_dtype ct, cudaStream_t stream) {
+  DeviceInfo di;
+  fp8bs_status st = device_info(&di);
+  if (st != FP8BS_OK) return st;
+  const int tiles = p.num_m_tiles * p.num_n_tiles;
+  const int grid = tiles < di.num_sms ? tiles : di.num_sms;
+  auto run = [&](auto kernel) -> fp8bs_status {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kGemmSmemBytes)) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
+    kernel<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p, ta, tb);
+    return launch_status();
+  };
+  const bool bf16 = ct == FP8BS_BF16;
+  if (sb_kind == kSbBlock)
+    return bf16 ? run(fp8bs_gemm_kernel<kGrouped, kSbBlock, true>)
+                : run(fp8bs_gemm_kernel<kGrouped, kSbBlock, false>);
+  return bf16 ? run(fp8bs_gemm_kernel<kGrouped, kSbPerCol, true>)
+              : run(fp8bs_gemm_kernel<kGrouped, kSbPerCol, false>);
+}
+
+void fill_scale_strides(GemmParams& p, fp8bs_bscale mode, int64_t ldsb) {
+  p.ldsb = ldsb;
+  if (mode == FP8BS_SB_BLOCK_NK) {
+    p.sb_k_stride = 1;
+    p.sb_n_stride = ldsb;
+  } else if (mode == FP8BS_SB_BLOCK_KN) {
+    p.sb_k_stride = ldsb;
+    p.sb_n_stride = 1;
+  } else {
+    p.sb_k_stride = 0;
+    p.sb_n_stride = 0;
+  }
+}
+
+// Zero-fill of C for K == 0 (the empty contraction).
+__global__ void zero_fill_kernel(unsigned char* C, int64_t row_bytes, int64_t ld_bytes,
+                                 int64_t rows) {
+  const int64_t r = blockIdx.x;
+  if (r >= rows) return;
+  uint4* dst = reinterpret_cast<uint4*>(C + r * ld_bytes);
+  for (int64_t i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+}
+
+fp8bs_status zero_fill(void* C, fp8bs_dtype ct, int64_t rows, int64_t N, int64_t ldc,
+                       cudaStream_t stream) {
+  // N is a multiple of 16 here, so a row is a whole number of 16-byte words.
+  int64_t done = 0;
+  while (done < rows) {
+    const int64_t chunk = rows - done < 65535 * 1024 ? rows - done : 65535 * 1024;
+    const int64_t esz = static_cast<int64_t>(dtype_size(ct));
+    zero_fill_kernel<<<static_cast<unsigned>(chunk), 256, 0, stream>>>(
+        static_cast<unsigned char*>(C) + done * ldc * esz, N * esz, ldc * esz, chunk);
+    fp8bs_status st = launch_status();
+    if (st != FP8BS_OK) return st;
+    done += chunk;
+  }
+  return FP8BS_OK;
+}
+
+}  // namespace
+}  // namespace fp8bs
+
+using namespace fp8bs;
+
+extern "C" {
+
+fp8bs_status fp8bs_quant_act_1x128(const void* x, fp8bs_dtype xt, int64_t M, int64_t K,
+                                   int64_t ldx, uint8_t* q, int64_t ldq, float* s, int64_t lds,
+                                   void* stream) {
+  if (M < 0 || K < 0 || !valid_dtype(xt)) return FP8BS_ERR_INVALID_ARG;
+  if (K % 128 != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (M == 0 || K == 0) return FP8BS_OK;
+  if (M * (K / 128) > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+  if (x == nullptr || q == nullptr || s == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (ldx < K || ldq < K || lds < M) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(q, 16) || (ldx * static_cast<int64_t>(dtype_size(xt))) % 16 ||
+      ldq % 16 || !aligned(s, 4))
+    return FP8BS_ERR_MISALIGNED;
+  DeviceInfo di;
+  fp8bs_status st = device_info(&di);
+  if (st != FP8BS_OK) return st;
+  constexpr int kUnroll = 4;
+  const int64_t tiles = M * (K / 128);
+  const int64_t tiles_per_block = (xt == FP8BS_BF16 ? 2 : 1) * kUnroll * 8;
+  int64_t blocks = (tiles + tiles_per_block - 1) / tiles_per_block;
+  const int64_t max_blocks = static_cast<int64_t>(di.num_sms) * 8;
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (xt == FP8BS_BF16)
+    quant_1x128_kernel<__nv_bfloat16, kUnroll><<<static_cast<unsigned>(blocks), 256, 0,
+                                                 as_stream(stream)>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M),
+        static_cast<uint32_t>(K / 128), ldx, q, ldq, s, lds);
+  else
+    quant_1x128_kernel<float, kUnroll><<<static_cast<unsigned>(blocks), 256, 0,
+                                         as_stream(stream)>>>(
+        static_cast<const float*>(x), static_cast<uint32_t>(M), static_cast<uint32_t>(K / 128),
+        ldx, q, ldq, s, lds);
+  return launch_status();
+}
+
+fp8bs_status fp8bs_quant_act_128x1(const void* x, fp8bs_dtype xt, int64_t T, int64_t C,
+                                   int64_t ldx, uint8_t* qT, int64_t ldq, float* s, int64_t lds,
+                                   void* stream) {
+  if (T < 0 || C < 0 || !valid_dtype(xt)) return FP8BS_ERR_INVALID_ARG;
+  if (T % 128 != 0 || C % 16 != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (T == 0 || C == 0) return FP8BS_OK;
+  if (T / 128 > 65535) return FP8BS_ERR_UNSUPPORTED;
+  if (x == nullptr || qT == nullptr || s == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (ldx < C || ldq < T || lds < C) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(qT, 16) || (ldx * static_cast<int64_t>(dtype_size(xt))) % 16 ||
+      ldq % 16 || !aligned(s, 4))
+    return FP8BS_ERR_MISALIGNED;
+  const int64_t cb = xt == FP8BS_BF16 ? 128 : 64;
+  dim3 grid(static_cast<unsigned>((C + cb - 1) / cb), static_cast<unsigned>(T / 128));
+  if (xt == FP8BS_BF16)
+    quant_128x1_kernel<__nv_bfloat16><<<grid, 256, 0, as_stream(stream)>>>(
+        static_cast<const __nv_bfloat16*>(x), C, ldx, qT, ldq, s, lds);
+  else
+    quant_128x1_kernel<float><<<grid, 256, 0, as_stream(stream)>>>(static_cast<const float*>(x),
+                                                                   C, ldx, qT, ldq, s, lds);
+  return launch_status();
+}
+
+fp8bs_status fp8bs_quant_w_128x128(const void* w, fp8bs_dtype wt, int64_t R, int64_t C,
+                                   int64_t ldw, uint8_t* q, int64_t ldq, uint8_t* qT,
+                                   int64_t ldqT, float* s, int64_t lds, void* stream) {
+  if (R < 0 || C < 0 || !valid_dtype(wt)) return FP8BS_ERR_INVALID_ARG;
+  if (R % 128 != 0 || C % 128 != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (R == 0 || C == 0) return FP8BS_OK;
+  if (R / 128 > 65535 || C / 128 > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+  if (w == nullptr || s == nullptr || (q == nullptr && qT == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (ldw < C || (q && ldq < C) || (qT && ldqT < R) || lds < C / 128) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || (ldw * static_cast<int64_t>(dtype_size(wt))) % 16 || !aligned(s, 4))
+    return FP8BS_ERR_MISALIGNED;
+  if (q && (!aligned(q, 16) || ldq % 16)) return FP8BS_ERR_MISALIGNED;
+  if (qT && (!aligned(qT, 16) || ldqT % 16)) return FP8BS_ERR_MISALIGNED;
+  dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R / 128));
+  const size_t smem = 128 * 128 * dtype_size(wt);
+  if (wt == FP8BS_BF16) {
+    quant_128x128_kernel<__nv_bfloat16><<<grid, 256, smem, as_stream(stream)>>>(
+        static_cast<const __nv_bfloat16*>(w), ldw, q, ldq, qT, ldqT, s, lds);
+  } else {
+    if (cudaFuncSetAttribute(quant_128x128_kernel<float>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
+    quant_128x128_kernel<float><<<grid, 256, smem, as_stream(stream)>>>(
+        static_cast<const float*>(w), ldw, q, ldq, qT, ldqT, s, lds);
+  }
+  return launch_status();
+}
+
+fp8bs_status fp8bs_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                        const float* sa, int64_t ldsa, const uint8_t* B, int64_t ldb,
+                        const float* sb, fp8bs_bscale sb_mode, int64_t ldsb, void* C,
+                        fp8bs_dtype ct, int64_t ldc, void* stream) {
+  fp8bs_status st = check_gemm(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc);
+  if (st != FP8BS_OK || M == 0 || N == 0) return st;
+  if (K == 0) return zero_fill(C, ct, M, N, ldc, as_stream(stream));
+  CUtensorMap ta, tb;
+  if ((st = make_map_2d(&ta, A, K, M, lda, kBM)) != FP8BS_OK) return st;
+  if ((st = make_map_3d(&tb, B, K, N, 1, ldb, kBN)) != FP8BS_OK) return st;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(N);
+  p.KB = static_cast<int32_t>(K / kBK);
+  p.num_m_tiles = static_cast<int32_t>((M + kBM - 1) / kBM);
+  p.num_n_tiles = static_cast<int32_t>((N + kBN - 1) / kBN);
+  p.E = 1;
+  p.sa = sa;
+  p.ldsa = ldsa;
+  p.sb = sb;
+  fill_scale_strides(p, sb_mode, ldsb);
+  p.sb_e_stride = 0;
+  p.C = C;
+  p.ldc = ldc;
+  p.offsets = nullptr;
+  return launch_gemm<false>(p, ta, tb, sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct,
+                            as_stream(stream));
+}
+
+fp8bs_status fp8bs_grouped_gemm(int32_t E, const int32_t* offsets, int64_t M_cap, int64_t N,
+                                int64_t K, const uint8_t* A, int64_t lda, const float* sa,
+                                int64_t ldsa, const uint8_t* B, int64_t ldb, const float* sb,
+                                fp8bs_bscale sb_mode, int64_t ldsb, int64_t sb_estride, void* C,
+                                fp8bs_dtype ct, int64_t ldc, void* stream) {
+  if (E < 1 || E > kMaxExperts || offsets == nullptr || !aligned(offsets, 4))
+    return FP8BS_ERR_INVALID_ARG;
+  if (M_cap < 0 || M_cap % 128 != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (sb_estride < 0) return FP8BS_ERR_INVALID_ARG;
+  fp8bs_status st =
+      check_gemm(M_cap, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc);
+  if (st != FP8BS_OK || M_cap == 0 || N == 0) return st;
+  if (sb_mode == FP8BS_SB_PERCOL && sb_estride % 4 != 0) return FP8BS_ERR_MISALIGNED;
+  if (K == 0) return FP8BS_ERR_UNSUPPORTED;  // expert rows are only known on the device
+  CUtensorMap ta, tb;
+  if ((st = make_map_2d(&ta, A, K, M_cap, lda, kBM)) != FP8BS_OK) return st;
+  if ((st = make_map_3d(&tb, B, K, N, E, ldb, kBN)) != FP8BS_OK) return st;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(M_cap);
+  p.N = static_cast<int32_t>(N);
+  p.KB = static_cast<int32_t>(K / kBK);
+  p.num_m_tiles = static_cast<int32_t>(M_cap / kBM);
+  p.num_n_tiles = static_cast<int32_t>((N + kBN - 1) / kBN);
+  p.E = E;
+  p.sa = sa;
+  p.ldsa = ldsa;
+  p.sb = sb;
+  fill_scale_strides(p, sb_mode, ldsb);
+  p.sb_e_stride = sb_estride;
+  p.C = C;
+  p.ldc = ldc;
+  p.offsets = offsets;
+  return launch_gemm<true>(p, ta, tb, sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct,
+                           as_stream(stream));
+}
+
+fp8bs_status fp8bs_sync_status(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof(word)) != cudaSuccess)
+    return FP8BS_ERR_CUDA;
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
+    if (word & kDevErrTimeout) return FP8BS_ERR_DEVICE_TIMEOUT;
+    return FP8BS_ERR_DEVICE_BAD_OFFSETS;
+  }
+  return FP8BS_OK;
+}
+
+const char* fp8bs_status_string(fp8bs_status status) {
+  switch (status) {
+    case FP8BS_OK: return "ok";
+    case FP8BS_ERR_INVALID_ARG: return "invalid argument";
+    case FP8BS_ERR_MISALIGNED: return "misaligned pointer or leading dimension";
+    case FP8BS_ERR_UNSUPPORTED: return "unsupported shape";
+    case FP8BS_ERR_CUDA: return "CUDA error";
+    case FP8BS_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case FP8BS_ERR_DEVICE_BAD_OFFSETS: return "grouped GEMM offsets failed device validation";
+  }
+  return "unknown status";
+}
+
+fp8bs_status fp8bs_debug_timeout_probe(int64_t limit_ns, void* stream) {
+  if (limit_ns < 1000 || limit_ns > 10000000000LL) return FP8BS_ERR_INVALID_ARG;
+  fp8bs_timeout_probe_kernel<<<1, 32, 0, as_stream(stream)>>>(static_cast<uint64_t>(limit_ns));
+  return launch_status();
+}
+
+}  // extern "C"

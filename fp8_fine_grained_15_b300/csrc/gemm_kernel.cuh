@@ -1,0 +1,407 @@
+// Block-scaled FP8 GEMM with promotion of every 128-deep K-slab into FP32
+// registers on CUDA cores.
+//
+// Method: "Should Fixing Deepseek Take 60 Steps?", Figure 6 passage (Fprop,
+// Dgrad, Wgrad in FP8; FP8 inputs, BF16 / FP32 outputs) and Figure 7 (a)
+// passage (1x128 activation tiles, 128x128 weight blocks); untitled page at
+// jp-study.kr, Figure 7 (b) passage (partial sums promoted to FP32 on CUDA
+// cores with the scales applied; MMA and promotion overlap so the tensor cores
+// stay busy).
+//
+// B300 design (one CTA per SM, persistent):
+//   warp 0      TMA producer: A tile 128x128 B and B tile 256x128 B per K-slab,
+//               128-byte swizzle, into a kStages-deep shared-memory ring.
+//   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32)
+//               per slab into one of two TMEM slab buffers (256 columns each);
+//               commits release the smem stage and publish the slab.
+//   warps 2,3   idle (they complete the producer warpgroup)
+//   warps 4..11 promotion + epilogue: tcgen05.ld the slab (32 rows x 128
+//               columns per warp), acc += P * (sa[row] * sb) in FP32 registers
+//               (packed f32x2 FMAs), release the TMEM buffer; after the last
+//               slab convert and store the 128 x 256 output tile.
+// The double-buffered TMEM slab lets the tensor cores run slab k+1 while the
+// CUDA cores promote slab k -- the overlap the pages get from two WGMMA
+// warpgroups on H800.
+#pragma once
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fp8bs {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 128;  // one promotion slab, one scale group
+constexpr int kStages = 4;
+constexpr int kStageABytes = kBM * kBK;
+constexpr int kStageBBytes = kBN * kBK;
+constexpr int kStageBytes = kStageABytes + kStageBBytes;
+constexpr int kTmemCols = 512;         // two slab buffers of kBN columns
+constexpr int kGemmThreads = 384;      // 3 warpgroups
+constexpr int kEpiWarps = 8;
+// Register split: launch budget 168 x 384; the producer warpgroup gives up all
+// but 40 per thread so the two promotion warpgroups can hold 232 each
+// (128 x 40 + 256 x 232 = 64512 = 168 x 384).
+constexpr uint32_t kProducerRegs = 40;
+constexpr uint32_t kEpilogueRegs = 232;
+static_assert(128 * kProducerRegs + 256 * kEpilogueRegs <= 168 * kGemmThreads,
+              "register split exceeds the launch budget");
+constexpr int kMaxExperts = 1024;
+
+enum SbKind : int { kSbBlock = 0, kSbPerCol = 1 };
+
+struct GemmParams {
+  int32_t M;            // rows of A / C (M_cap for the grouped call)
+  int32_t N;
+  int32_t KB;           // K / 128
+  int32_t num_m_tiles;
+  int32_t num_n_tiles;
+  int32_t E;            // experts (1 for the dense call)
+  const float* sa;      // sa[kb*ldsa + row]
+  int64_t ldsa;
+  const float* sb;
+  int64_t sb_k_stride;  // block modes: element stride per K-slab
+  int64_t sb_n_stride;  // block modes: element stride per 128-column block
+  int64_t ldsb;         // per-column mode: stride per K-slab
+  int64_t sb_e_stride;  // per expert
+  void* C;
+  int64_t ldc;          // elements
+  const int32_t* offsets;  // grouped: device offsets[E+1]
+};
+
+struct GemmSmem {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t bad_offsets;
+  int32_t rows_valid;  // grouped: offsets[E]
+  int32_t offsets[kMaxExperts + 1];
+};
+
+constexpr size_t kGemmSmemBytes =
+    1024 /* alignment slack */ + static_cast<size_t>(kStages) * kStageBytes + sizeof(GemmSmem);
+
+struct TileCoord {
+  int32_t m0, n0, e;
+  bool valid;
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ TileCoord tile_coord(int t, const GemmParams& p, const GemmSmem& sm) {
+  TileCoord c;
+  const int mt = t % p.num_m_tiles;
+  const int nt = t / p.num_m_tiles;
+  c.m0 = mt * kBM;
+  c.n0 = nt * kBN;
+  c.e = 0;
+  c.valid = true;
+  if constexpr (kGrouped) {
+    if (c.m0 >= sm.rows_valid) {
+      c.valid = false;
+    } else {
+      // last e with offsets[e] <= m0 (offsets validated non-decreasing)
+      int lo = 0, hi = p.E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sm.offsets[mid] <= c.m0) lo = mid; else hi = mid - 1;
+      }
+      c.e = lo;
+    }
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// acc[j] += P[j] * scale for 16 columns held as 16 raw fp32 words.
+__device__ __forceinline__ void promote16(float2* acc, const uint32_t (&r)[16], float2 sc2) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    acc[i] = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                        sc2, acc[i]);
+}
+
+// acc[j] += (P[j] * sb[j]) * sa for 16 columns with per-column B scales.
+__device__ __forceinline__ void promote16_percol(float2* acc, const uint32_t (&r)[16],
+                                                 const float* __restrict__ sbv, float2 sa2) {
+  const float4* sb4 = reinterpret_cast<const float4*>(sbv);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 b = __ldg(sb4 + i);
+    const float2 p0 = make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]));
+    const float2 p1 = make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+    acc[2 * i] = __ffma2_rn(__fmul2_rn(p0, make_float2(b.x, b.y)), sa2, acc[2 * i]);
+    acc[2 * i + 1] = __ffma2_rn(__fmul2_rn(p1, make_float2(b.z, b.w)), sa2, acc[2 * i + 1]);
+  }
+}
+
+template <bool kGrouped, int kSb, bool kOutBf16>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    fp8bs_gemm_kernel(const __grid_constant__ GemmParams p,
+                      const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_b) {
+  extern __shared__ __align__(1024) unsigned char gemm_smem_raw[];
+  // 1024-byte aligned operand ring (the 128-byte swizzle atoms need it)
+  const uint32_t raw_addr = smem_u32(gemm_smem_raw);
+  unsigned char* ring = gemm_smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  GemmSmem& sm = *reinterpret_cast<GemmSmem*>(ring + static_cast<size_t>(kStages) * kStageBytes);
+  const uint32_t ring_addr = smem_u32(ring);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.tfull[b], 1);
+      mbar_init(&sm.tempty[b], kEpiWarps);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    sm.bad_offsets = 0;
+    sm.rows_valid = p.M;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if constexpr (kGrouped) {
+    // Stage and validate the expert offsets (every CTA, so none depends on another).
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) sm.offsets[i] = p.offsets[i];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      bool ok = sm.offsets[0] == 0;
+      for (int e = 0; e < p.E && ok; ++e)
+        ok = sm.offsets[e + 1] >= sm.offsets[e] && (sm.offsets[e + 1] % kBM) == 0;
+      ok = ok && sm.offsets[p.E] <= p.M;
+      if (!ok) {
+        sm.bad_offsets = 1;
+        if (blockIdx.x == 0) atomicOr(&g_device_error, kDevErrBadOffsets);
+      } else {
+        sm.rows_valid = sm.offsets[p.E];
+      }
+    }
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sm.tmem_base;
+  const bool skip_all = kGrouped && sm.bad_offsets;
+
+  if (warp < 4) {
+    regs_dealloc<kProducerRegs>();
+  if (!skip_all && warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA
+    const uint64_t policy = l2_policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0, parity_mask = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const TileCoord tc = tile_coord<kGrouped>(t, p, sm);
+      if (!tc.valid) continue;
+      for (int kb = 0; kb < p.KB; ++kb) {
+        if (!bounded_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) goto producer_done;
+        mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
+        const uint32_t sa_addr = ring_addr + stage * kStageBytes;
+        tma_load_2d(sa_addr, &tmap_a, kb * kBK, tc.m0, &sm.full[stage], policy);
+        tma_load_3d(sa_addr + kStageABytes, &tmap_b, kb * kBK, tc.n0, tc.e, &sm.full[stage],
+                    policy);
+        issued_mask |= 1u << stage;
+        parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  producer_done:
+    // Every load issued must land before the CTA may exit.
+    for (int s = 0; s < kStages; ++s)
+      if (issued_mask & (1u << s))
+        bounded_wait_noabort(&sm.full[s], (parity_mask >> s) & 1u, kSpinLimitNs);
+  } else if (!skip_all && warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA
+    constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
+    int stage = 0, buf = 0;
+    uint32_t phase = 0, tphase = 0;
+    bool issued = false;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const TileCoord tc = tile_coord<kGrouped>(t, p, sm);
+      if (!tc.valid) continue;
+      for (int kb = 0; kb < p.KB; ++kb) {
+        if (!bounded_wait(&sm.full[stage], phase, abort_flag)) goto mma_done;
+        if (!bounded_wait(&sm.tempty[buf], tphase ^ 1u, abort_flag)) goto mma_done;
+        tc_fence_after();
+        const uint32_t a_addr = ring_addr + stage * kStageBytes;
+        const uint64_t adesc = smem_desc_k_sw128(a_addr);
+        const uint64_t bdesc = smem_desc_k_sw128(a_addr + kStageABytes);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 32; ++kk)  // 32 bytes = 32 E4M3 values per MMA
+          mma_f8f6f4(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+        mma_commit(&sm.empty[stage]);
+        mma_commit(&sm.tfull[buf]);
+        issued = true;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++buf == 2) {
+          buf = 0;
+          tphase ^= 1u;
+        }
+      }
+    }
+  mma_done:
+    if (issued) {  // all MMAs must finish before TMEM is released
+      mma_commit(&sm.drain);
+      bounded_wait_noabort(&sm.drain, 0, kSpinLimitNs);
+    }
+  }
+  } else {
+    regs_alloc<kEpilogueRegs>();
+    if (!skip_all) {
+    // ------------------------------------------------- promotion + epilogue
+    const int g = warp & 3;          // TMEM lane group (rows 32g .. 32g+31)
+    const int h = (warp - 4) >> 2;   // column half (0: 0..127, 1: 128..255)
+    int buf = 0;
+    uint32_t tphase = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const TileCoord tc = tile_coord<kGrouped>(t, p, sm);
+      if (!tc.valid) continue;
+      const int row = tc.m0 + g * 32 + lane;
+      const bool row_ok = row < p.M;
+      const int col0 = tc.n0 + h * 128;
+      const bool cols_ok = col0 < p.N;
+      const float* sbe = p.sb + static_cast<int64_t>(tc.e) * p.sb_e_stride;
+      float2 acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
+
+      auto load_sa = [&](int kb) -> float {
+        return (row_ok && kb < p.KB) ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ldsa + row)
+                                     : 0.0f;
+      };
+      auto load_sb = [&](int kb) -> float {
+        if constexpr (kSb == kSbBlock) {
+          return (cols_ok && kb < p.KB)
+                     ? __ldg(sbe + static_cast<int64_t>(kb) * p.sb_k_stride +
+                             static_cast<int64_t>(col0 / 128) * p.sb_n_stride)
+                     : 0.0f;
+        } else {
+          return 0.0f;
+        }
+      };
+      float sa_cur = load_sa(0), sb_cur = load_sb(0);
+      for (int kb = 0; kb < p.KB; ++kb) {
+        const float sa_nxt = load_sa(kb + 1), sb_nxt = load_sb(kb + 1);
+        if (!bounded_wait(&sm.tfull[buf], tphase, abort_flag)) goto epilogue_done;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) +
+                               static_cast<uint32_t>(buf * kBN + h * 128);
+        uint32_t ra[16], rb[16];
+        tmem_ld16(taddr, ra);
+        tmem_wait_ld(ra);
+        if constexpr (kSb == kSbBlock) {
+          const float sc = sa_cur * sb_cur;
+          const float2 sc2 = make_float2(sc, sc);
+#pragma unroll
+          for (int c = 0; c < 8; c += 2) {
+            tmem_ld16(taddr + (c + 1) * 16, rb);
+            promote16(acc + c * 8, ra, sc2);
+            tmem_wait_ld(rb);
+            if (c + 2 < 8) tmem_ld16(taddr + (c + 2) * 16, ra);
+            promote16(acc + (c + 1) * 8, rb, sc2);
+            if (c + 2 < 8) tmem_wait_ld(ra);
+          }
+        } else {
+          const float2 sa2 = make_float2(sa_cur, sa_cur);
+          const float* sbk = sbe + static_cast<int64_t>(kb) * p.ldsb + col0;
+          const bool ok = cols_ok;
+#pragma unroll
+          for (int c = 0; c < 8; c += 2) {
+            tmem_ld16(taddr + (c + 1) * 16, rb);
+            if (ok && col0 + c * 16 < p.N) promote16_percol(acc + c * 8, ra, sbk + c * 16, sa2);
+            tmem_wait_ld(rb);
+            if (c + 2 < 8) tmem_ld16(taddr + (c + 2) * 16, ra);
+            if (ok && col0 + (c + 1) * 16 < p.N)
+              promote16_percol(acc + (c + 1) * 8, rb, sbk + (c + 1) * 16, sa2);
+            if (c + 2 < 8) tmem_wait_ld(ra);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tempty[buf]);
+        if (++buf == 2) {
+          buf = 0;
+          tphase ^= 1u;
+        }
+        sa_cur = sa_nxt;
+        sb_cur = sb_nxt;
+      }
+      // ---- epilogue: this thread's row, 128 columns
+      if (row_ok && cols_ok) {
+        if constexpr (kOutBf16) {
+          __nv_bfloat16* crow = reinterpret_cast<__nv_bfloat16*>(p.C) +
+                                static_cast<int64_t>(row) * p.ldc + col0;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {  // 8 columns per 16-byte store
+            if (kSb == kSbPerCol && col0 + c * 8 >= p.N) break;
+            uint4 o;
+            o.x = pack_bf16x2(acc[4 * c].x, acc[4 * c].y);
+            o.y = pack_bf16x2(acc[4 * c + 1].x, acc[4 * c + 1].y);
+            o.z = pack_bf16x2(acc[4 * c + 2].x, acc[4 * c + 2].y);
+            o.w = pack_bf16x2(acc[4 * c + 3].x, acc[4 * c + 3].y);
+            *reinterpret_cast<uint4*>(crow + c * 8) = o;
+          }
+        } else {
+          float* crow = reinterpret_cast<float*>(p.C) + static_cast<int64_t>(row) * p.ldc + col0;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {  // 4 columns per 16-byte store
+            if (kSb == kSbPerCol && col0 + c * 4 >= p.N) break;
+            *reinterpret_cast<float4*>(crow + c * 4) =
+                make_float4(acc[2 * c].x, acc[2 * c].y, acc[2 * c + 1].x, acc[2 * c + 1].y);
+          }
+        }
+      }
+    }
+  epilogue_done:;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// One CTA waits on a barrier that nothing arrives at, with a time limit; the
+// wait gives up, records a timeout in the device error word and returns.
+__global__ void fp8bs_timeout_probe_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) bounded_wait_noabort(&bar, 0, limit_ns);
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,173 @@
+/*
+ * fp8bs -- fine-grained FP8 quantization and block-scaled FP8 GEMM for B300
+ * (sm_103a).  Plain C ABI: device pointers, sizes and a CUDA stream passed as
+ * an opaque pointer.  No call allocates memory.
+ *
+ * What the operations compute comes from the FP8 mixed-precision training
+ * scheme described on the pages (a DeepSeek-V3-style framework):
+ *   - "Should Fixing Deepseek Take 60 Steps?", Figure 7 (a) passage: activations
+ *     are grouped and scaled per 1x128 tile (one token, 128 channels); weights
+ *     per 128x128 block (128 input channels x 128 output channels).
+ *   - same page, max-abs scaling passage: each group is aligned to the FP8 range
+ *     by mapping its largest magnitude onto the largest FP8 value; the max-abs
+ *     is taken online per tile / block (page at why-be.why-be.co.kr, online
+ *     amax passage).
+ *   - untitled page at jp-study.kr, hybrid-format passage: E4M3 on all tensors.
+ *   - "Should Fixing Deepseek Take 60 Steps?", Figure 6 passage: Fprop, Dgrad and
+ *     Wgrad run in FP8, take FP8 inputs and produce BF16 or FP32.
+ *   - untitled page at jp-study.kr, Figure 7 (b) passage: partial results are
+ *     promoted to FP32 registers on CUDA cores, where the scales are applied.
+ *
+ * Quantization (bit-exact contract, all three granularities):
+ *   amax = max |x| over the tile (x widened to fp32 exactly);
+ *   r    = fl32(448 / amax);  if r is not finite (amax == 0, or amax below
+ *          448/FLT_MAX) the tile is treated as all-zero: s = r = 1;
+ *   s    = fl32(amax / 448)   (the stored scale; x ~= dec(q) * s);
+ *   q    = E4M3(fl32(x * r)), round to nearest even, finite overflow saturates
+ *          to +-448, the sign of zero is kept.
+ *   Codes are OCP E4M3FN bytes (bias 7, 0x7E = 448, 0x7F = NaN).
+ *   NaN / Inf inputs are outside the contract.
+ *
+ * GEMM (promotion interval = one 128-deep K-slab):
+ *   C[i][j] = sum_kb ( sum_{k in slab kb} dec(A[i][k]) * dec(B[j][k]) )
+ *             * sa[kb][i] * sb(kb, j)
+ *   Each slab's partial sum is produced by the tensor cores in FP32 and added
+ *   into FP32 accumulators on CUDA cores with the two scales applied.
+ *
+ * Error behaviour: every call checks its arguments on the host before any
+ * launch and returns a status; nothing is launched on error.  Launch failures
+ * return FP8BS_ERR_CUDA.  Kernels never trap: a device-side wait that runs past
+ * its limit, or invalid device-resident group offsets, is recorded in a device
+ * error word that fp8bs_sync_status() reports and clears.  All calls are
+ * asynchronous on the given stream (NULL = legacy default stream).
+ *
+ * Layout conventions: matrices are row-major; "ld" arguments are leading
+ * dimensions in elements of that matrix's type (bytes for E4M3 codes).
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp8bs_status {
+  FP8BS_OK = 0,
+  FP8BS_ERR_INVALID_ARG = 1,     /* null pointer, negative size, ld too small */
+  FP8BS_ERR_MISALIGNED = 2,      /* pointer / leading dimension alignment */
+  FP8BS_ERR_UNSUPPORTED = 3,     /* shape outside the supported set (e.g. K % 128) */
+  FP8BS_ERR_CUDA = 4,            /* CUDA runtime / launch error */
+  FP8BS_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up on a device-side wait */
+  FP8BS_ERR_DEVICE_BAD_OFFSETS = 6 /* grouped GEMM offsets failed device validation */
+} fp8bs_status;
+
+typedef enum fp8bs_dtype { FP8BS_F32 = 0, FP8BS_BF16 = 1 } fp8bs_dtype;
+
+/* Layout of the B-operand scales of fp8bs_gemm / fp8bs_grouped_gemm.
+ *   BLOCK_NK: sb[(n/128)*ldsb + k/128]  one scale per 128x128 block, ldsb >= K/128
+ *   BLOCK_KN: sb[(k/128)*ldsb + n/128]  one scale per 128x128 block, ldsb >= N/128
+ *   PERCOL  : sb[(k/128)*ldsb + n]      one scale per column per 128-deep slab
+ *                                       (128x1 tiles along K), ldsb >= N        */
+typedef enum fp8bs_bscale {
+  FP8BS_SB_BLOCK_NK = 0,
+  FP8BS_SB_BLOCK_KN = 1,
+  FP8BS_SB_PERCOL = 2
+} fp8bs_bscale;
+
+/* 1x128 activation quantizer (one scale per token per 128 channels).
+ *   x  [M x K] fp32 or bf16 (xt), row stride ldx >= K elements.
+ *   q  [M x K] E4M3 codes, row stride ldq >= K bytes.
+ *   s  [K/128][lds] fp32, s[kb*lds + m], lds >= M (M-contiguous: the layout the
+ *      GEMM reads for its A operand).
+ * Requirements: K % 128 == 0 (UNSUPPORTED); x, q 16-byte aligned and
+ * ldx*sizeof(xt), ldq multiples of 16 (MISALIGNED); s 4-byte aligned.
+ * M == 0 or K == 0 is a no-op.  Caller owns all buffers. */
+fp8bs_status fp8bs_quant_act_1x128(const void* x, fp8bs_dtype xt, int64_t M, int64_t K,
+                                   int64_t ldx, uint8_t* q, int64_t ldq, float* s,
+                                   int64_t lds, void* stream);
+
+/* 128x1 activation quantizer (one scale per channel per 128 tokens), output
+ * transposed so that tokens are contiguous: the K-major operand layout of the
+ * Wgrad GEMM (contraction over tokens).
+ *   x  [T x C] fp32 or bf16, row stride ldx >= C.
+ *   qT [C x T] E4M3 codes, qT[c*ldq + t], ldq >= T.
+ *   s  [T/128][lds] fp32, s[tb*lds + c], lds >= C.
+ * Requirements: T % 128 == 0, C % 16 == 0 (UNSUPPORTED); x, qT 16-byte aligned,
+ * ldx*sizeof(xt) and ldq multiples of 16 (MISALIGNED).
+ * The codes equal those of fp8bs_quant_act_1x128 applied to x transposed. */
+fp8bs_status fp8bs_quant_act_128x1(const void* x, fp8bs_dtype xt, int64_t T, int64_t C,
+                                   int64_t ldx, uint8_t* qT, int64_t ldq, float* s,
+                                   int64_t lds, void* stream);
+
+/* 128x128 weight quantizer (one scale per 128 x 128 block).
+ *   w  [R x C] fp32 or bf16, row stride ldw >= C.
+ *   q  [R x C] E4M3 codes (ldq >= C) -- may be NULL;
+ *   qT [C x R] the same codes transposed (ldqT >= R) -- may be NULL; not both.
+ *   s  [R/128][lds] fp32, s[rb*lds + cb], lds >= C/128.
+ * With a weight stored as W [K_in x N_out]: qT is the B operand of Fprop
+ * (rows N_out, K-major over K_in, scales BLOCK_KN) and q is the B operand of
+ * Dgrad (rows K_in, K-major over N_out, scales BLOCK_NK).
+ * Requirements: R % 128 == 0 and C % 128 == 0 (UNSUPPORTED); w, q, qT 16-byte
+ * aligned, leading dimensions multiples of 16 bytes (MISALIGNED). */
+fp8bs_status fp8bs_quant_w_128x128(const void* w, fp8bs_dtype wt, int64_t R, int64_t C,
+                                   int64_t ldw, uint8_t* q, int64_t ldq, uint8_t* qT,
+                                   int64_t ldqT, float* s, int64_t lds, void* stream);
+
+/* Block-scaled FP8 GEMM  C[M x N] = A[M x K] * B[N x K]^T  (both K-major).
+ *   A  E4M3 codes, row stride lda >= K bytes; sa[kb*ldsa + i] fp32, ldsa >= M
+ *      (the layout fp8bs_quant_act_1x128 / _128x1 write).
+ *   B  E4M3 codes, row stride ldb >= K bytes; sb in layout sb_mode (above).
+ *   C  [M x N] fp32 or bf16 (ct), row stride ldc >= N; bf16 is rounded to
+ *      nearest even from the FP32 accumulator.
+ * Fprop  : A = Xq (1x128), B = WqT, sb = Sw as BLOCK_KN, C bf16.
+ * Dgrad  : A = dYq (1x128), B = Wq, sb = Sw as BLOCK_NK, C bf16.
+ * Wgrad  : A = XqT (128x1), B = dYqT (128x1), sb = S_dY as PERCOL, C fp32.
+ * Requirements: K % 128 == 0; N % 128 == 0 for BLOCK modes, N % 8 == 0 for
+ * PERCOL (UNSUPPORTED); A, B, C 16-byte aligned; lda, ldb, ldc*sizeof(ct)
+ * multiples of 16 (MISALIGNED); sa, sb 4-byte aligned.  M, N == 0: no-op;
+ * K == 0 writes zeros.  Any M >= 1 is allowed (the last row tile is ragged). */
+fp8bs_status fp8bs_gemm(int64_t M, int64_t N, int64_t K,
+                        const uint8_t* A, int64_t lda, const float* sa, int64_t ldsa,
+                        const uint8_t* B, int64_t ldb, const float* sb, fp8bs_bscale sb_mode,
+                        int64_t ldsb, void* C, fp8bs_dtype ct, int64_t ldc, void* stream);
+
+/* Grouped block-scaled FP8 GEMM for MoE experts: expert e owns rows
+ * offsets[e] .. offsets[e+1]-1 of A and C and multiplies them by B[e]:
+ *   C[i][:] = A[i][:] * B[e]^T with the scales sa (rows) and sb + e*sb_estride.
+ *   offsets  DEVICE array of E+1 int32: offsets[0] == 0, non-decreasing,
+ *            multiples of 128, offsets[E] <= M_cap.  Validated on the device;
+ *            a violation writes nothing and is reported by fp8bs_sync_status()
+ *            as FP8BS_ERR_DEVICE_BAD_OFFSETS.  Empty experts are allowed.
+ *   A [M_cap x K] (lda), sa[kb*ldsa + i] (ldsa >= M_cap);
+ *   B [E][N][ldb] codes, expert stride N*ldb bytes;
+ *   sb per expert in layout sb_mode with stride ldsb, experts sb_estride apart;
+ *   C [M_cap x N] (ldc); rows at or past offsets[E] are left untouched.
+ * Requirements: 1 <= E <= 1024, M_cap % 128 == 0, plus those of fp8bs_gemm. */
+fp8bs_status fp8bs_grouped_gemm(int32_t E, const int32_t* offsets, int64_t M_cap, int64_t N,
+                                int64_t K, const uint8_t* A, int64_t lda, const float* sa,
+                                int64_t ldsa, const uint8_t* B, int64_t ldb, const float* sb,
+                                fp8bs_bscale sb_mode, int64_t ldsb, int64_t sb_estride,
+                                void* C, fp8bs_dtype ct, int64_t ldc, void* stream);
+
+/* Synchronize the stream, then report (and clear) the device error word of the
+ * current device: FP8BS_ERR_DEVICE_TIMEOUT, FP8BS_ERR_DEVICE_BAD_OFFSETS,
+ * FP8BS_ERR_CUDA for a sticky CUDA error, else FP8BS_OK. */
+fp8bs_status fp8bs_sync_status(void* stream);
+
+/* Static string naming a status code. */
+const char* fp8bs_status_string(fp8bs_status status);
+
+/* Test hook for the failure path: launch one CTA that waits on a barrier no
+ * one arrives at, with a limit of limit_ns nanoseconds (1e3 .. 1e10).  The
+ * wait gives up, records a timeout in the device error word and returns, so
+ * fp8bs_sync_status() then reports FP8BS_ERR_DEVICE_TIMEOUT.  No trap, no
+ * hang.  Not part of the method (the pages have no counterpart). */
+fp8bs_status fp8bs_debug_timeout_probe(int64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

@@ -1,0 +1,108 @@
+"""Grouped (MoE expert) GEMM parity against the oracle applied expert by
+expert, plus device-side offset validation."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_fine_grained_15_b300 as fb
+import oracle
+import workloads as wl
+from gpu_helpers import DEV, assert_gemm_close, oracle_input, to_dev_f32, to_dev_u8
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_grouped(offsets, Aq, sa, Bq, sb, mode, out=torch.bfloat16, sentinel=3.0):
+    M_cap = Aq.shape[0]
+    N = Bq.shape[1]
+    C = torch.full((M_cap, N), sentinel, dtype=out, device=DEV)
+    off = torch.tensor(np.asarray(offsets, np.int32), device=DEV)
+    fb.fp8bs_grouped_gemm(off, to_dev_u8(Aq), to_dev_f32(sa), to_dev_u8(Bq), to_dev_f32(sb),
+                          mode, C)
+    st = fb.fp8bs_sync_status()
+    return st, C.float().cpu().numpy().astype(np.float64)
+
+
+def _experts(E, N, K, seed):
+    Bq, sbs = [], []
+    for e in range(E):
+        w = wl.random_matrix((K, N), seed=seed + e, dtype=torch.bfloat16, std=0.02)
+        _, WqT, sw = oracle.quant_w_128x128(oracle_input(w))
+        Bq.append(WqT)
+        sbs.append(sw)
+    return np.stack(Bq), np.stack(sbs)          # [E x N x K], [E x K/128 x N/128]
+
+
+def test_grouped_small_with_empty_experts():
+    E, N, K = 4, 384, 512
+    offsets = [0, 128, 128, 384, 512]            # expert 1 empty
+    M_cap = 640                                  # rows 512.. belong to nobody
+    a = wl.random_matrix((M_cap, K), seed=41, dtype=torch.bfloat16)
+    Aq, sa = oracle.quant_act_1x128(oracle_input(a))
+    Bq, sb = _experts(E, N, K, seed=42)
+    st, c = _run_grouped(offsets, Aq, sa, Bq, sb, fb.FP8BS_SB_BLOCK_KN)
+    assert st == fb.FP8BS_OK
+    c_ref, s_abs = oracle.grouped_gemm(offsets, Aq, sa, Bq, sb, oracle.SB_BLOCK_KN)
+    assert_gemm_close(c[:512], c_ref[:512], s_abs[:512], True, "grouped small")
+    assert np.all(c[512:] == 3.0), "rows past offsets[E] must be untouched"
+
+
+def test_grouped_nk_scales_fp32_out():
+    E, N, K = 3, 256, 384
+    offsets = [0, 256, 384, 384]                 # last expert empty
+    a = wl.random_matrix((384, K), seed=43, dtype=torch.bfloat16)
+    Aq, sa = oracle.quant_act_1x128(oracle_input(a))
+    Bq, sb = _experts(E, N, K, seed=44)
+    sb_nk = np.ascontiguousarray(np.transpose(sb, (0, 2, 1)))
+    st, c = _run_grouped(offsets, Aq, sa, Bq, sb_nk, fb.FP8BS_SB_BLOCK_NK, out=torch.float32)
+    assert st == fb.FP8BS_OK
+    c_ref, s_abs = oracle.grouped_gemm(offsets, Aq, sa, Bq, sb_nk, oracle.SB_BLOCK_NK)
+    assert_gemm_close(c, c_ref, s_abs, False, "grouped NK fp32")
+
+
+@pytest.mark.parametrize("offsets", [[0, 100, 256], [0, 256, 128], [128, 256, 384],
+                                     [0, 128, 1024]])
+def test_grouped_bad_offsets_reported_and_nothing_written(offsets):
+    E, N, K = 2, 256, 128
+    Aq = np.zeros((512, K), np.uint8)
+    sa = np.ones((1, 512), np.float32)
+    Bq = np.zeros((E, N, K), np.uint8)
+    sb = np.ones((E, 1, 2), np.float32)
+    st, c = _run_grouped(offsets, Aq, sa, Bq, sb, fb.FP8BS_SB_BLOCK_KN)
+    assert st == fb.FP8BS_ERR_DEVICE_BAD_OFFSETS
+    assert np.all(c == 3.0)
+    assert fb.fp8bs_sync_status() == fb.FP8BS_OK      # the status was cleared
+
+
+def test_grouped_moe_up_projection_sampled():
+    """32 experts, 16384 routed rows with Zipf(1.1) counts padded to 128,
+    K = 7168, N = 4096 per expert."""
+    counts, offsets, x, w = wl.grouped_moe()
+    E, K, N = w.shape
+    Aq, sa = oracle.quant_act_1x128(oracle_input(x))
+    Bq = np.empty((E, N, K), np.uint8)
+    sb = np.empty((E, K // 128, N // 128), np.float32)
+    for e in range(E):
+        _, Bq[e], sb[e] = oracle.quant_w_128x128(oracle_input(w[e]), with_transpose=True)
+    st, c = _run_grouped(offsets, Aq, sa, Bq, sb, fb.FP8BS_SB_BLOCK_KN)
+    assert st == fb.FP8BS_OK
+    rng = np.random.default_rng(7)
+    rows, cols = [], []
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        real = r0 + int(counts[e])
+        for n0 in range(0, N, 256):               # one element per (m-tile, n-tile)
+            for m0 in range(r0, r1, 128):
+                rows.append(rng.integers(m0, m0 + 128))
+                cols.append(rng.integers(n0, n0 + 256))
+        if real < r1:                              # a padding row must come out as 0
+            rows.append(r1 - 1)
+            cols.append(rng.integers(0, N))
+    rows = np.array(rows, np.int64)
+    cols = np.array(cols, np.int64)
+    c_ref, s_abs = oracle.grouped_gemm_elements(offsets, Aq, sa, Bq, sb, oracle.SB_BLOCK_KN,
+                                                rows, cols)
+    assert_gemm_close(c[rows, cols], c_ref, s_abs, True, "grouped MoE")
+    pad_rows = [int(offsets[e]) + int(counts[e]) for e in range(E)
+                if int(offsets[e]) + int(counts[e]) < int(offsets[e + 1])]
+    assert np.all(c[pad_rows] == 0)
