@@ -193,6 +193,21 @@ fp8bs_status zero_fill(void* C, fp8bs_dtype ct, int64_t rows, int64_t N, int64_t
   return FP8BS_OK;
 }
 
+// Grid-stride launch of the 1x128 quantizer: at most 8 blocks of 256 threads per SM.
+template <typename TIn, int kUnroll>
+void launch_quant_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                        int64_t ldq, float* s, int64_t lds, const DeviceInfo& di,
+                        cudaStream_t stream) {
+  const int64_t tiles = M * (K / 128);
+  const int64_t tiles_per_block = 8 /* warps */ * 8 /* tiles per warp step */ * kUnroll;
+  int64_t blocks = (tiles + tiles_per_block - 1) / tiles_per_block;
+  const int64_t max_blocks = static_cast<int64_t>(di.num_sms) * 8;
+  if (blocks > max_blocks) blocks = max_blocks;
+  quant_1x128_kernel<TIn, kUnroll><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const TIn*>(x), static_cast<uint32_t>(M), static_cast<uint32_t>(K / 128), ldx,
+      q, ldq, s, lds);
+}
+
 }  // namespace
 }  // namespace fp8bs
 
@@ -215,22 +230,10 @@ fp8bs_status fp8bs_quant_act_1x128(const void* x, fp8bs_dtype xt, int64_t M, int
   DeviceInfo di;
   fp8bs_status st = device_info(&di);
   if (st != FP8BS_OK) return st;
-  constexpr int kUnroll = 4;
-  const int64_t tiles = M * (K / 128);
-  const int64_t tiles_per_block = (xt == FP8BS_BF16 ? 2 : 1) * kUnroll * 8;
-  int64_t blocks = (tiles + tiles_per_block - 1) / tiles_per_block;
-  const int64_t max_blocks = static_cast<int64_t>(di.num_sms) * 8;
-  if (blocks > max_blocks) blocks = max_blocks;
   if (xt == FP8BS_BF16)
-    quant_1x128_kernel<__nv_bfloat16, kUnroll><<<static_cast<unsigned>(blocks), 256, 0,
-                                                 as_stream(stream)>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M),
-        static_cast<uint32_t>(K / 128), ldx, q, ldq, s, lds);
+    launch_quant_1x128<__nv_bfloat16, 2>(x, M, K, ldx, q, ldq, s, lds, di, as_stream(stream));
   else
-    quant_1x128_kernel<float, kUnroll><<<static_cast<unsigned>(blocks), 256, 0,
-                                         as_stream(stream)>>>(
-        static_cast<const float*>(x), static_cast<uint32_t>(M), static_cast<uint32_t>(K / 128),
-        ldx, q, ldq, s, lds);
+    launch_quant_1x128<float, 1>(x, M, K, ldx, q, ldq, s, lds, di, as_stream(stream));
   return launch_status();
 }
 

@@ -42,10 +42,10 @@ constexpr int kTmemCols = 512;         // two slab buffers of kBN columns
 constexpr int kGemmThreads = 384;      // 3 warpgroups
 constexpr int kEpiWarps = 8;
 // Register split: launch budget 168 x 384; the producer warpgroup gives up all
-// but 40 per thread so the two promotion warpgroups can hold 232 each
-// (128 x 40 + 256 x 232 = 64512 = 168 x 384).
-constexpr uint32_t kProducerRegs = 40;
-constexpr uint32_t kEpilogueRegs = 232;
+// but 56 per thread so the two promotion warpgroups can hold 224 each
+// (128 x 56 + 256 x 224 = 64512 = 168 x 384).
+constexpr uint32_t kProducerRegs = 56;
+constexpr uint32_t kEpilogueRegs = 224;
 static_assert(128 * kProducerRegs + 256 * kEpilogueRegs <= 168 * kGemmThreads,
               "register split exceeds the launch budget");
 constexpr int kMaxExperts = 1024;
@@ -82,6 +82,9 @@ struct GemmSmem {
   int32_t bad_offsets;
   int32_t rows_valid;  // grouped: offsets[E]
   int32_t offsets[kMaxExperts + 1];
+  // per-column B scales of the current and the next slab, one copy per
+  // promotion warp (its 128 columns)
+  alignas(16) float sb_stage[kEpiWarps][2][128];
 };
 
 constexpr size_t kGemmSmemBytes =
@@ -122,21 +125,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// acc[j] += P[j] * scale for 16 columns held as 16 raw fp32 words.
-__device__ __forceinline__ void promote16(float2* acc, const uint32_t (&r)[16], float2 sc2) {
+// acc[j] += P[j] * scale for 32 columns held as 32 raw fp32 words.
+__device__ __forceinline__ void promote32(float2* acc, const uint32_t (&r)[32], float2 sc2) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 16; ++i)
     acc[i] = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
                         sc2, acc[i]);
 }
 
-// acc[j] += (P[j] * sb[j]) * sa for 16 columns with per-column B scales.
-__device__ __forceinline__ void promote16_percol(float2* acc, const uint32_t (&r)[16],
-                                                 const float* __restrict__ sbv, float2 sa2) {
+// acc[j] += (P[j] * sb[j]) * sa for 32 columns; sb[] read from shared memory
+// (every lane reads the same addresses: broadcast).
+__device__ __forceinline__ void promote32_percol(float2* acc, const uint32_t (&r)[32],
+                                                 const float* sbv, float2 sa2) {
   const float4* sb4 = reinterpret_cast<const float4*>(sbv);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 b = __ldg(sb4 + i);
+  for (int i = 0; i < 8; ++i) {
+    const float4 b = sb4[i];
     const float2 p0 = make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]));
     const float2 p1 = make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
     acc[2 * i] = __ffma2_rn(__fmul2_rn(p0, make_float2(b.x, b.y)), sa2, acc[2 * i]);
@@ -307,41 +311,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       };
       float sa_cur = load_sa(0), sb_cur = load_sb(0);
+      // per-column mode: this warp's 128 B scales of a slab, staged in smem
+      float* sb_mine = &sm.sb_stage[warp - 4][0][0];
+      auto fetch_sb_cols = [&](int kb) -> float4 {
+        const int c = col0 + lane * 4;
+        return (kb < p.KB && c < p.N)
+                   ? __ldg(reinterpret_cast<const float4*>(sbe + static_cast<int64_t>(kb) * p.ldsb + c))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      };
+      if constexpr (kSb == kSbPerCol) {
+        const float4 v = fetch_sb_cols(0);
+        reinterpret_cast<float4*>(sb_mine)[lane] = v;
+        __syncwarp();
+      }
       for (int kb = 0; kb < p.KB; ++kb) {
         const float sa_nxt = load_sa(kb + 1), sb_nxt = load_sb(kb + 1);
+        float4 sbc_nxt;
+        if constexpr (kSb == kSbPerCol) sbc_nxt = fetch_sb_cols(kb + 1);
         if (!bounded_wait(&sm.tfull[buf], tphase, abort_flag)) goto epilogue_done;
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) +
                                static_cast<uint32_t>(buf * kBN + h * 128);
-        uint32_t ra[16], rb[16];
-        tmem_ld16(taddr, ra);
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr, ra);
         tmem_wait_ld(ra);
         if constexpr (kSb == kSbBlock) {
           const float sc = sa_cur * sb_cur;
           const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-          for (int c = 0; c < 8; c += 2) {
-            tmem_ld16(taddr + (c + 1) * 16, rb);
-            promote16(acc + c * 8, ra, sc2);
+          for (int c = 0; c < 4; c += 2) {
+            tmem_ld32(taddr + (c + 1) * 32, rb);
+            promote32(acc + c * 16, ra, sc2);
             tmem_wait_ld(rb);
-            if (c + 2 < 8) tmem_ld16(taddr + (c + 2) * 16, ra);
-            promote16(acc + (c + 1) * 8, rb, sc2);
-            if (c + 2 < 8) tmem_wait_ld(ra);
+            if (c + 2 < 4) tmem_ld32(taddr + (c + 2) * 32, ra);
+            promote32(acc + (c + 1) * 16, rb, sc2);
+            if (c + 2 < 4) tmem_wait_ld(ra);
           }
         } else {
+          // columns past N carry zero scales (and zero products), so no guard is needed
           const float2 sa2 = make_float2(sa_cur, sa_cur);
-          const float* sbk = sbe + static_cast<int64_t>(kb) * p.ldsb + col0;
-          const bool ok = cols_ok;
+          const float* sbs = sb_mine + (kb & 1) * 128;
 #pragma unroll
-          for (int c = 0; c < 8; c += 2) {
-            tmem_ld16(taddr + (c + 1) * 16, rb);
-            if (ok && col0 + c * 16 < p.N) promote16_percol(acc + c * 8, ra, sbk + c * 16, sa2);
+          for (int c = 0; c < 4; c += 2) {
+            tmem_ld32(taddr + (c + 1) * 32, rb);
+            promote32_percol(acc + c * 16, ra, sbs + c * 32, sa2);
             tmem_wait_ld(rb);
-            if (c + 2 < 8) tmem_ld16(taddr + (c + 2) * 16, ra);
-            if (ok && col0 + (c + 1) * 16 < p.N)
-              promote16_percol(acc + (c + 1) * 8, rb, sbk + (c + 1) * 16, sa2);
-            if (c + 2 < 8) tmem_wait_ld(ra);
+            if (c + 2 < 4) tmem_ld32(taddr + (c + 2) * 32, ra);
+            promote32_percol(acc + (c + 1) * 16, rb, sbs + (c + 1) * 32, sa2);
+            if (c + 2 < 4) tmem_wait_ld(ra);
           }
+          reinterpret_cast<float4*>(sb_mine + ((kb + 1) & 1) * 128)[lane] = sbc_nxt;
+          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();

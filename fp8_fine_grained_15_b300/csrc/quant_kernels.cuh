@@ -88,60 +88,72 @@ __device__ __forceinline__ uint32_t e4m3x4(const float* f, float r) {
 }
 
 // ---------------------------------------------------------------- 1 x 128
-// Each 128-element tile is handled by kLanes lanes holding one 16-byte vector
-// each (16 lanes for bf16, 32 for fp32); a warp covers 32/kLanes tiles per step
-// and kUnroll steps per iteration, so every lane keeps kUnroll independent
-// 16-byte loads in flight.  Tiles are numbered row-major (m, kb).
+// Four lanes share a 128-element tile, 32 elements each, so the per-tile work
+// (two IEEE divisions, two shuffle steps, index arithmetic) is spread over 32
+// elements per lane.  Load i of a lane covers elements [i*4v + l*v, +v) of its
+// tile (v = 16 bytes of input), so the four lanes of a tile read 64 contiguous
+// bytes per instruction.  A warp covers 8 tiles per step and kUnroll steps per
+// iteration; tiles are numbered row-major (m, kb).
 template <typename TIn, int kUnroll>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const TIn* __restrict__ x, uint32_t M,
                                                           uint32_t KB, int64_t ldx,
                                                           uint8_t* __restrict__ q, int64_t ldq,
                                                           float* __restrict__ s, int64_t lds) {
-  constexpr int kVec = Vec16<TIn>::kN;
-  constexpr int kLanes = 128 / kVec;
-  constexpr int kTilesPerStep = 32 / kLanes;
-  constexpr int kTilesPerIter = kTilesPerStep * kUnroll;
+  constexpr int kVec = Vec16<TIn>::kN;         // elements per 16-byte load
+  constexpr int kLoads = 128 / (4 * kVec);     // 16-byte loads per lane per tile
+  constexpr int kTilesPerIter = 8 * kUnroll;
   const int lane = threadIdx.x & 31;
-  const int sub = lane / kLanes;
-  const int li = lane % kLanes;
+  const int sub = lane >> 2;                   // tile within the warp step
+  const int l = lane & 3;                      // lane within the tile
   const uint32_t total = M * KB;
   const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t num_warps = (gridDim.x * blockDim.x) >> 5;
 
   for (uint32_t base = warp_id * kTilesPerIter; base < total; base += num_warps * kTilesPerIter) {
-    uint4 v[kUnroll];
+    uint4 v[kUnroll][kLoads];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t t = base + u * kTilesPerStep + sub;
+      const uint32_t t = base + u * 8 + sub;
       if (t < total) {
         const uint32_t m = t / KB, kb = t - m * KB;
-        v[u] = ld_stream16(x + static_cast<int64_t>(m) * ldx + kb * 128 + li * kVec);
+        const TIn* src = x + static_cast<int64_t>(m) * ldx + kb * 128 + l * kVec;
+#pragma unroll
+        for (int i = 0; i < kLoads; ++i) v[u][i] = ld_stream16(src + i * 4 * kVec);
       } else {
-        v[u] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < kLoads; ++i) v[u][i] = make_uint4(0, 0, 0, 0);
       }
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t t = base + u * kTilesPerStep + sub;
-      float f[kVec];
-      Vec16<TIn>::widen(v[u], f);
+      const uint32_t t = base + u * 8 + sub;
       float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < kVec; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      for (int i = 0; i < kLoads; ++i) {
+        float f[kVec];
+        Vec16<TIn>::widen(v[u][i], f);
 #pragma unroll
-      for (int o = kLanes / 2; o > 0; o >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        for (int j = 0; j < kVec; ++j) amax = fmaxf(amax, fabsf(f[j]));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       float sc, r;
       tile_scale(amax, sc, r);
       if (t < total) {
         const uint32_t m = t / KB, kb = t - m * KB;
-        uint8_t* dst = q + static_cast<int64_t>(m) * ldq + kb * 128 + li * kVec;
-        if constexpr (kVec == 8) {
-          *reinterpret_cast<uint2*>(dst) = make_uint2(e4m3x4(f, r), e4m3x4(f + 4, r));
-        } else {
-          *reinterpret_cast<uint32_t*>(dst) = e4m3x4(f, r);
+        uint8_t* dst = q + static_cast<int64_t>(m) * ldq + kb * 128 + l * kVec;
+#pragma unroll
+        for (int i = 0; i < kLoads; ++i) {
+          float f[kVec];
+          Vec16<TIn>::widen(v[u][i], f);
+          if constexpr (kVec == 8) {
+            *reinterpret_cast<uint2*>(dst + i * 4 * kVec) =
+                make_uint2(e4m3x4(f, r), e4m3x4(f + 4, r));
+          } else {
+            *reinterpret_cast<uint32_t*>(dst + i * 4 * kVec) = e4m3x4(f, r);
+          }
         }
-        if (li == 0) s[static_cast<int64_t>(kb) * lds + m] = sc;
+        if (l == 0) s[static_cast<int64_t>(kb) * lds + m] = sc;
       }
     }
   }
