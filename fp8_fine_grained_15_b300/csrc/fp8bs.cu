@@ -193,6 +193,14 @@ fp8bs_status zero_fill(void* C, fp8bs_dtype ct, int64_t rows, int64_t N, int64_t
   return FP8BS_OK;
 }
 
+// Ask for the maximum shared-memory carveout once per kernel, so that several
+// staging CTAs fit on an SM (the default carveout left room for only three).
+template <typename K>
+void prefer_max_shared(K kernel) {
+  cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       static_cast<int>(cudaSharedmemCarveoutMaxShared));
+}
+
 // Grid-stride launch of the 1x128 quantizer: at most 8 blocks of 256 threads per SM.
 template <typename TIn, int kUnroll>
 void launch_quant_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
@@ -251,12 +259,15 @@ fp8bs_status fp8bs_quant_act_128x1(const void* x, fp8bs_dtype xt, int64_t T, int
     return FP8BS_ERR_MISALIGNED;
   const int64_t cb = xt == FP8BS_BF16 ? 128 : 64;
   dim3 grid(static_cast<unsigned>((C + cb - 1) / cb), static_cast<unsigned>(T / 128));
-  if (xt == FP8BS_BF16)
+  if (xt == FP8BS_BF16) {
+    prefer_max_shared(quant_128x1_kernel<__nv_bfloat16>);
     quant_128x1_kernel<__nv_bfloat16><<<grid, 256, 0, as_stream(stream)>>>(
         static_cast<const __nv_bfloat16*>(x), C, ldx, qT, ldq, s, lds);
-  else
+  } else {
+    prefer_max_shared(quant_128x1_kernel<float>);
     quant_128x1_kernel<float><<<grid, 256, 0, as_stream(stream)>>>(static_cast<const float*>(x),
                                                                    C, ldx, qT, ldq, s, lds);
+  }
   return launch_status();
 }
 
@@ -276,6 +287,7 @@ fp8bs_status fp8bs_quant_w_128x128(const void* w, fp8bs_dtype wt, int64_t R, int
   dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R / 128));
   const size_t smem = 128 * 128 * dtype_size(wt);
   if (wt == FP8BS_BF16) {
+    prefer_max_shared(quant_128x128_kernel<__nv_bfloat16>);
     quant_128x128_kernel<__nv_bfloat16><<<grid, 256, smem, as_stream(stream)>>>(
         static_cast<const __nv_bfloat16*>(w), ldw, q, ldq, qT, ldqT, s, lds);
   } else {
@@ -283,6 +295,7 @@ fp8bs_status fp8bs_quant_w_128x128(const void* w, fp8bs_dtype wt, int64_t R, int
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return FP8BS_ERR_CUDA;
+    prefer_max_shared(quant_128x128_kernel<float>);
     quant_128x128_kernel<float><<<grid, 256, smem, as_stream(stream)>>>(
         static_cast<const float*>(w), ldw, q, ldq, qT, ldqT, s, lds);
   }

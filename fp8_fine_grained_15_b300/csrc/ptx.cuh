@@ -123,6 +123,35 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void* tmap,
       : "memory");
 }
 
+// Same, multicast: the box lands at the same shared-memory offset in every CTA
+// of cta_mask and signals the mbarrier at the same offset in each of them.
+__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst_smem, const void* tmap,
+                                                      int32_t c0, int32_t c1, int32_t c2,
+                                                      uint64_t* bar, uint16_t cta_mask,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6, %7;" ::"r"(dst_smem),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+      "h"(cta_mask), "l"(policy)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA in the cluster; release/acquire ordering.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
 // L2 policy: keep operand tiles resident (they are re-read by other CTAs).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
@@ -179,6 +208,15 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
+      : "memory");
+}
+
+// Same, arriving on the barrier at the same offset in every CTA of cta_mask.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 

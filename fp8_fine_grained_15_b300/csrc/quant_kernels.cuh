@@ -18,6 +18,8 @@
 
 #include <cstdint>
 
+#include "ptx.cuh"
+
 namespace fp8bs {
 
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
@@ -160,24 +162,28 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const TIn* __restrict_
 }
 
 // ---------------------------------------------------------------- 128 x 1
-// One CTA per (128 tokens) x (256 bytes of channels): the block is staged in
-// shared memory with coalesced 16-byte row loads, then each thread owns one
-// channel and a contiguous run of tokens: it reduces the amax (combined across
-// the token parts through shared memory), quantizes, and writes its tokens as
-// contiguous 16-byte runs of the transposed output.
+// One CTA per (128 tokens) x (256 bytes of channels).  The block is staged in
+// shared memory with cp.async (no register round trip, L1 bypassed).  Each
+// thread then owns one 32-bit channel group (two bf16 channels or one fp32
+// channel) and 32 consecutive tokens: 32 conflict-free word reads, a
+// per-channel partial amax combined across the four token parts through shared
+// memory, then 32 codes per channel written as two 16-byte runs of the
+// transposed output.
 template <typename TIn>
-__global__ void __launch_bounds__(256) quant_128x1_kernel(const TIn* __restrict__ x, int64_t C,
-                                                          int64_t ldx, uint8_t* __restrict__ qT,
-                                                          int64_t ldq, float* __restrict__ s,
-                                                          int64_t lds) {
+__global__ void __launch_bounds__(256, 4) quant_128x1_kernel(const TIn* __restrict__ x, int64_t C,
+                                                             int64_t ldx, uint8_t* __restrict__ qT,
+                                                             int64_t ldq, float* __restrict__ s,
+                                                             int64_t lds) {
   constexpr int kVec = Vec16<TIn>::kN;
   constexpr int kCB = 256 / sizeof(TIn);       // channels per CTA (256 bytes per row)
   constexpr int kVecPerRow = kCB / kVec;       // 16
   constexpr int kRowsPerPass = 256 / kVecPerRow;
-  constexpr int kLoads = 128 / kRowsPerPass;   // 16-byte loads per thread
-  constexpr int kParts = 256 / kCB;            // token parts per channel
-  constexpr int kTok = 128 / kParts;           // tokens per thread
-  __shared__ __align__(16) TIn tile[128][kCB];
+  constexpr int kLoads = 128 / kRowsPerPass;   // 16-byte copies per thread
+  constexpr int kCh = 4 / sizeof(TIn);         // channels per 32-bit word
+  constexpr int kGroups = kCB / kCh;           // 64 word columns
+  constexpr int kParts = 256 / kGroups;        // 4 token parts
+  constexpr int kTok = 128 / kParts;           // 32 tokens per thread
+  __shared__ __align__(16) uint32_t tile[128][kGroups];
   __shared__ float part_amax[kParts][kCB];
 
   const int64_t tb = blockIdx.y;
@@ -187,86 +193,125 @@ __global__ void __launch_bounds__(256) quant_128x1_kernel(const TIn* __restrict_
     const int vc = tid % kVecPerRow;
     const int r0 = tid / kVecPerRow;
     const int64_t col = c0 + vc * kVec;
-    uint4 v[kLoads];
 #pragma unroll
     for (int i = 0; i < kLoads; ++i) {
       const int64_t row = tb * 128 + r0 + i * kRowsPerPass;
-      v[i] = (col < C) ? ld_stream16(x + row * ldx + col) : make_uint4(0, 0, 0, 0);
+      uint32_t* dst = &tile[r0 + i * kRowsPerPass][vc * 4];
+      if (col < C) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                     "l"(x + row * ldx + col)
+                     : "memory");
+      } else {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+      }
     }
-#pragma unroll
-    for (int i = 0; i < kLoads; ++i)
-      *reinterpret_cast<uint4*>(&tile[r0 + i * kRowsPerPass][vc * kVec]) = v[i];
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   }
   __syncthreads();
 
-  const int c = tid % kCB;
-  const int part = tid / kCB;
-  float f[kTok];
-  float amax = 0.0f;
+  const int g = tid % kGroups;
+  const int part = tid / kGroups;
+  uint32_t w[kTok];
+  float amax[kCh];
+#pragma unroll
+  for (int k = 0; k < kCh; ++k) amax[k] = 0.0f;
 #pragma unroll
   for (int t = 0; t < kTok; ++t) {
-    f[t] = widen1<TIn>(tile[part * kTok + t][c]);
-    amax = fmaxf(amax, fabsf(f[t]));
+    w[t] = tile[part * kTok + t][g];
+    if constexpr (kCh == 2) {
+      amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(w[t] << 16)));
+      amax[1] = fmaxf(amax[1], fabsf(__uint_as_float(w[t] & 0xFFFF0000u)));
+    } else {
+      amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(w[t])));
+    }
   }
-  part_amax[part][c] = amax;
+#pragma unroll
+  for (int k = 0; k < kCh; ++k) part_amax[part][g * kCh + k] = amax[k];
   __syncthreads();
 #pragma unroll
-  for (int p = 0; p < kParts; ++p) amax = fmaxf(amax, part_amax[p][c]);
-  float sc, r;
-  tile_scale(amax, sc, r);
-  if (c0 + c < C) {
-    uint8_t* dst = qT + (c0 + c) * ldq + tb * 128 + part * kTok;
+  for (int k = 0; k < kCh; ++k) {
+    float a = part_amax[0][g * kCh + k];
 #pragma unroll
-    for (int t = 0; t < kTok; t += 16) {
-      uint4 o;
-      o.x = e4m3x4(f + t, r);
-      o.y = e4m3x4(f + t + 4, r);
-      o.z = e4m3x4(f + t + 8, r);
-      o.w = e4m3x4(f + t + 12, r);
-      *reinterpret_cast<uint4*>(dst + t) = o;
+    for (int p = 1; p < kParts; ++p) a = fmaxf(a, part_amax[p][g * kCh + k]);
+    float sc, r;
+    tile_scale(a, sc, r);
+    const int64_t c = c0 + g * kCh + k;
+    if (c < C) {
+      uint8_t* dst = qT + c * ldq + tb * 128 + part * kTok;
+#pragma unroll
+      for (int t = 0; t < kTok; t += 16) {
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float f[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t wv = w[t + 4 * j + i];
+            f[i] = __uint_as_float(kCh == 1 ? wv : (k == 0 ? (wv << 16) : (wv & 0xFFFF0000u)));
+          }
+          o[j] = e4m3x4(f, r);
+        }
+        *reinterpret_cast<uint4*>(dst + t) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      if (part == 0) s[tb * lds + c] = sc;
     }
-    if (part == 0) s[tb * lds + c0 + c] = sc;
   }
 }
 
 // -------------------------------------------------------------- 128 x 128
-// One CTA per 128 x 128 block.  Each thread loads its 16-byte vectors once;
-// the block amax is reduced through warp shuffles and shared memory.  The
-// row-major codes are written from registers; the transposed copy is read
-// column-wise from the staged block (dynamic shared memory: 32 KB for bf16,
-// 64 KB for fp32).  Both copies come from the same multiply and conversion.
+// One CTA per 128 x 128 block, staged in shared memory with cp.async (32 KB
+// for bf16, 64 KB for fp32).  Each thread owns one 32-bit word column (two
+// bf16 channels or one fp32 channel) over a run of rows: it reduces its part of
+// the block amax from those words (then warp shuffles + shared memory), and
+// later re-reads them 16 rows at a time to write that column's transposed
+// codes.  The row-major codes come from 16-byte shared-memory reads.  Both
+// copies use the same multiply and conversion, so they hold identical codes.
 template <typename TIn>
-__global__ void __launch_bounds__(256) quant_128x128_kernel(const TIn* __restrict__ w,
-                                                            int64_t ldw, uint8_t* __restrict__ q,
-                                                            int64_t ldq, uint8_t* __restrict__ qT,
-                                                            int64_t ldqT, float* __restrict__ s,
-                                                            int64_t lds) {
-  constexpr int kVec = Vec16<TIn>::kN;
-  constexpr int kVecPerRow = 128 / kVec;       // 16 (bf16) or 32 (fp32)
-  constexpr int kRowsPerPass = 256 / kVecPerRow;
-  constexpr int kLoads = 128 / kRowsPerPass;   // 8 or 16
+__global__ void __launch_bounds__(256, 5) quant_128x128_kernel(const TIn* __restrict__ w,
+                                                               int64_t ldw,
+                                                               uint8_t* __restrict__ q,
+                                                               int64_t ldq,
+                                                               uint8_t* __restrict__ qT,
+                                                               int64_t ldqT,
+                                                               float* __restrict__ s,
+                                                               int64_t lds) {
+  constexpr int kVec = Vec16<TIn>::kN;                      // elements per 16 bytes
+  constexpr int kWordsPerRow = 128 * sizeof(TIn) / 4;       // 64 (bf16) or 128 (fp32)
+  constexpr int kVecPerRow = 128 / kVec;                    // 16 or 32
+  constexpr int kCh = 4 / sizeof(TIn);                      // channels per word
+  constexpr int kParts = 256 / kWordsPerRow;                // 4 or 2 row parts
+  constexpr int kRows = 128 / kParts;                       // 32 or 64 rows per thread
   extern __shared__ __align__(16) unsigned char dyn_smem[];
-  TIn(*tile)[128] = reinterpret_cast<TIn(*)[128]>(dyn_smem);
+  uint32_t* tile = reinterpret_cast<uint32_t*>(dyn_smem);   // [128][kWordsPerRow]
   __shared__ float warp_amax[8];
 
   const int64_t rb = blockIdx.y, cb = blockIdx.x;
   const int tid = threadIdx.x;
-  const int vc = tid % kVecPerRow;
-  const int r0 = tid / kVecPerRow;
-  const TIn* src = w + rb * 128 * ldw + cb * 128 + vc * kVec;
-  uint4 v[kLoads];
+  const TIn* src = w + rb * 128 * ldw + cb * 128;
 #pragma unroll
-  for (int i = 0; i < kLoads; ++i) v[i] = ld_stream16(src + (r0 + i * kRowsPerPass) * ldw);
+  for (int i = tid; i < 128 * kVecPerRow; i += 256) {
+    const int row = i / kVecPerRow, vc = i % kVecPerRow;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     smem_u32(tile + row * kWordsPerRow + vc * 4)),
+                 "l"(src + row * ldw + vc * kVec)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
 
+  const int g = tid % kWordsPerRow;
+  const int part = tid / kWordsPerRow;
+  const uint32_t* col = tile + part * kRows * kWordsPerRow + g;   // this thread's word column
   float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kLoads; ++i) {
-    float f[kVec];
-    Vec16<TIn>::widen(v[i], f);
-#pragma unroll
-    for (int j = 0; j < kVec; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    if (qT != nullptr)
-      *reinterpret_cast<uint4*>(&tile[r0 + i * kRowsPerPass][vc * kVec]) = v[i];
+#pragma unroll 8
+  for (int t = 0; t < kRows; ++t) {
+    const uint32_t v = col[t * kWordsPerRow];
+    if constexpr (kCh == 2) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(v << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(v & 0xFFFF0000u)));
+    } else {
+      amax = fmaxf(amax, fabsf(__uint_as_float(v)));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -279,36 +324,45 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const TIn* __restric
   tile_scale(amax, sc, r);
   if (tid == 0) s[rb * lds + cb] = sc;
 
-  if (q != nullptr) {
-    uint8_t* dst = q + rb * 128 * ldq + cb * 128 + vc * kVec;
+  if (qT != nullptr) {
+    // 16 rows at a time: 16 words -> 16 codes for each channel of the word
+    uint8_t* d0 = qT + (cb * 128 + g * kCh) * ldqT + rb * 128 + part * kRows;
+#pragma unroll 1
+    for (int t = 0; t < kRows; t += 16) {
+      uint32_t v[16];
 #pragma unroll
-    for (int i = 0; i < kLoads; ++i) {
+      for (int i = 0; i < 16; ++i) v[i] = col[(t + i) * kWordsPerRow];
+#pragma unroll
+      for (int k = 0; k < kCh; ++k) {
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float f[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t x = v[4 * j + i];
+            f[i] = __uint_as_float(kCh == 1 ? x : (k == 0 ? (x << 16) : (x & 0xFFFF0000u)));
+          }
+          o[j] = e4m3x4(f, r);
+        }
+        *reinterpret_cast<uint4*>(d0 + k * ldqT + t) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+  if (q != nullptr) {
+    uint8_t* dst = q + rb * 128 * ldq + cb * 128;
+#pragma unroll
+    for (int i = tid; i < 128 * kVecPerRow; i += 256) {
+      const int row = i / kVecPerRow, vc = i % kVecPerRow;
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + row * kWordsPerRow + vc * 4);
       float f[kVec];
-      Vec16<TIn>::widen(v[i], f);
-      uint8_t* d = dst + (r0 + i * kRowsPerPass) * ldq;
+      Vec16<TIn>::widen(v, f);
+      uint8_t* d = dst + row * ldq + vc * kVec;
       if constexpr (kVec == 8) {
         *reinterpret_cast<uint2*>(d) = make_uint2(e4m3x4(f, r), e4m3x4(f + 4, r));
       } else {
         *reinterpret_cast<uint32_t*>(d) = e4m3x4(f, r);
       }
-    }
-  }
-  if (qT != nullptr) {
-    // thread -> (column c, 64 consecutive rows)
-    const int c = tid & 127;
-    const int part = tid >> 7;
-    uint8_t* d = qT + (cb * 128 + c) * ldqT + rb * 128 + part * 64;
-#pragma unroll
-    for (int t = 0; t < 64; t += 16) {
-      float f[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) f[j] = widen1<TIn>(tile[part * 64 + t + j][c]);
-      uint4 o;
-      o.x = e4m3x4(f, r);
-      o.y = e4m3x4(f + 4, r);
-      o.z = e4m3x4(f + 8, r);
-      o.w = e4m3x4(f + 12, r);
-      *reinterpret_cast<uint4*>(d + t) = o;
     }
   }
 }
