@@ -461,8 +461,108 @@ def run_reference(args, rank, world, dist_on):
     }
 
 
+CASES = ("fprop", "dgrad", "wgrad", "grouped", "quant_1x128", "quant_128x1", "quant_128x128")
+
+
+def run_case(args):
+    """One kernel alone on its layer-sized operands (device-drawn, seeded):
+    `--warmup` untimed launches, then `--steps` launches timed one by one with
+    CUDA events.  This is the command the ncu captures under profiles/ run."""
+    import fp8_fine_grained_15_b300 as fb
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks = _peaks()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    T, K, N = TOKENS, HIDDEN, FFN
+    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device=dev)  # noqa: E731
+    f32 = lambda *s: torch.empty(*s, dtype=torch.float32, device=dev)  # noqa: E731
+    c = args.case
+    if c in ("fprop", "dgrad", "wgrad"):
+        x = torch.randn((T, K), device=dev, generator=gen).to(torch.bfloat16)
+        dy = (torch.randn((T, N), device=dev, generator=gen) * 1e-3).to(torch.bfloat16)
+        w = (torch.randn((K, N), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+        if c == "fprop":
+            A, sa, B, sb = u8(T, K), f32(K // 128, T), u8(N, K), f32(K // 128, N // 128)
+            fb.fp8bs_quant_act_1x128(x, A, sa, stream)
+            fb.fp8bs_quant_w_128x128(w, None, B, sb, stream)
+            out, mode = torch.empty((T, N), dtype=torch.bfloat16, device=dev), fb.FP8BS_SB_BLOCK_KN
+        elif c == "dgrad":
+            A, sa, B, sb = u8(T, N), f32(N // 128, T), u8(K, N), f32(K // 128, N // 128)
+            fb.fp8bs_quant_act_1x128(dy, A, sa, stream)
+            fb.fp8bs_quant_w_128x128(w, B, None, sb, stream)
+            out, mode = torch.empty((T, K), dtype=torch.bfloat16, device=dev), fb.FP8BS_SB_BLOCK_NK
+        else:
+            A, sa, B, sb = u8(K, T), f32(T // 128, K), u8(N, T), f32(T // 128, N)
+            fb.fp8bs_quant_act_128x1(x, A, sa, stream)
+            fb.fp8bs_quant_act_128x1(dy, B, sb, stream)
+            out, mode = torch.empty((K, N), dtype=torch.float32, device=dev), fb.FP8BS_SB_PERCOL
+        del x, dy, w
+        fn = lambda: fb.fp8bs_gemm(A, sa, B, sb, mode, out, stream)  # noqa: E731
+        amount, kind = 2.0 * T * K * N, "tensor"
+    elif c == "grouped":
+        counts = wl.zipf_counts()
+        offsets = wl.padded_offsets(counts)
+        E, Kg, Ng = wl.EXPERTS, wl.HIDDEN, wl.EXPERT_N
+        M_cap = int(offsets[-1])
+        A = torch.randint(0, 0x7E, (M_cap, Kg), dtype=torch.uint8, device=dev, generator=gen)
+        sa = torch.rand((Kg // 128, M_cap), device=dev, generator=gen) * 1e-2
+        B = torch.randint(0, 0x7E, (E, Ng, Kg), dtype=torch.uint8, device=dev, generator=gen)
+        sb = torch.rand((E, Kg // 128, Ng // 128), device=dev, generator=gen) * 1e-3
+        out = torch.empty((M_cap, Ng), dtype=torch.bfloat16, device=dev)
+        off = torch.tensor(offsets.astype(np.int32), device=dev)
+        fn = lambda: fb.fp8bs_grouped_gemm(off, A, sa, B, sb, fb.FP8BS_SB_BLOCK_KN, out,  # noqa: E731
+                                           stream)
+        amount, kind = 2.0 * int(counts.sum()) * Kg * Ng, "tensor"
+    else:
+        M = args.case_rows
+        if c == "quant_128x128":
+            x = (torch.randn((K, N), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+            q, qT, s = u8(K, N), u8(N, K), f32(K // 128, N // 128)
+            fn = lambda: fb.fp8bs_quant_w_128x128(x, q, qT, s, stream)  # noqa: E731
+            amount = quant_bytes(K * N, 2, True, True)
+        else:
+            x = torch.randn((M, K), device=dev, generator=gen).to(torch.bfloat16)
+            if c == "quant_1x128":
+                q, s = u8(M, K), f32(K // 128, M)
+                fn = lambda: fb.fp8bs_quant_act_1x128(x, q, s, stream)  # noqa: E731
+            else:
+                q, s = u8(K, M), f32(M // 128, K)
+                fn = lambda: fb.fp8bs_quant_act_128x1(x, q, s, stream)  # noqa: E731
+            amount = quant_bytes(M * K, 2)
+        kind = "hbm"
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > L2
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        fn()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(ev0.elapsed_time(ev1))
+    if fb.fp8bs_sync_status(stream) != 0:
+        raise RuntimeError("device error in case run")
+    med = statistics.median(ts)
+    if kind == "tensor":
+        ach, peak, unit = amount / (med * 1e-3) / 1e12, peaks["fp8_tflops"], "TFLOP/s"
+    else:
+        ach, peak, unit = amount / (med * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    return {"case": c, "launches": args.steps, "ms_median": round(med, 4),
+            "ms_min": round(min(ts), 4), "achieved": round(ach, 1), "unit": unit,
+            "peak": round(peak, 1), "frac": round(ach / peak, 4), "amount": amount}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="time one kernel alone (profiling command); no JSON bench line")
+    ap.add_argument("--case-rows", type=int, default=65536,
+                    help="rows of the activation quantizer cases")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
@@ -474,6 +574,9 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "fp8bs":
         ap.error("at least 3 warm-up steps")
+    if args.case is not None:
+        print(json.dumps(run_case(args)), flush=True)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -114,6 +114,7 @@ fp8bs_status check_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
   if (K % kBK != 0) return FP8BS_ERR_UNSUPPORTED;
   if (sb_mode == FP8BS_SB_PERCOL ? (N % 16 != 0) : (N % 128 != 0)) return FP8BS_ERR_UNSUPPORTED;
   if (M > INT_MAX - kBM || N > INT_MAX - kBN || K / kBK > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+  if (((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN) > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
   if (C == nullptr || ldc < N) return FP8BS_ERR_INVALID_ARG;
   if (!aligned(C, 16) || (ldc * static_cast<int64_t>(dtype_size(ct))) % 16 != 0)
     return FP8BS_ERR_MISALIGNED;

@@ -80,8 +80,11 @@ struct GemmSmem {
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t bad_offsets;
-  int32_t rows_valid;  // grouped: offsets[E]
+  int32_t num_tiles;   // dense: m tiles x n tiles; grouped: tile_base[E]
   int32_t offsets[kMaxExperts + 1];
+  // grouped: first tile index of each expert; expert e owns tiles
+  // tile_base[e] .. tile_base[e+1]-1, its m tiles fastest, then its n tiles
+  int32_t tile_base[kMaxExperts + 1];
   // per-column B scales of the current and the next slab, one copy per
   // promotion warp (its 128 columns)
   alignas(16) float sb_stage[kEpiWarps][2][128];
@@ -92,30 +95,31 @@ constexpr size_t kGemmSmemBytes =
 
 struct TileCoord {
   int32_t m0, n0, e;
-  bool valid;
 };
 
+// Output tile t of the persistent walk.  Dense: m tiles fastest, so the CTAs
+// of one wave share a few B panels and all of A stays in L2.  Grouped: expert
+// by expert, and within an expert its m tiles fastest, so an expert's rows of
+// A are re-read from L2 across its n tiles instead of from HBM.
 template <bool kGrouped>
 __device__ __forceinline__ TileCoord tile_coord(int t, const GemmParams& p, const GemmSmem& sm) {
   TileCoord c;
-  const int mt = t % p.num_m_tiles;
-  const int nt = t / p.num_m_tiles;
-  c.m0 = mt * kBM;
-  c.n0 = nt * kBN;
-  c.e = 0;
-  c.valid = true;
   if constexpr (kGrouped) {
-    if (c.m0 >= sm.rows_valid) {
-      c.valid = false;
-    } else {
-      // last e with offsets[e] <= m0 (offsets validated non-decreasing)
-      int lo = 0, hi = p.E - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (sm.offsets[mid] <= c.m0) lo = mid; else hi = mid - 1;
-      }
-      c.e = lo;
+    // owner: the last e with tile_base[e] <= t (it has at least one tile)
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sm.tile_base[mid] <= t) lo = mid; else hi = mid - 1;
     }
+    const int l = t - sm.tile_base[lo];
+    const int mte = (sm.offsets[lo + 1] - sm.offsets[lo]) / kBM;
+    c.e = lo;
+    c.m0 = sm.offsets[lo] + (l % mte) * kBM;
+    c.n0 = (l / mte) * kBN;
+  } else {
+    c.e = 0;
+    c.m0 = (t % p.num_m_tiles) * kBM;
+    c.n0 = (t / p.num_m_tiles) * kBN;
   }
   return c;
 }
@@ -162,7 +166,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     sm.bad_offsets = 0;
-    sm.rows_valid = p.M;
+    sm.num_tiles = p.num_m_tiles * p.num_n_tiles;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
@@ -186,17 +189,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Stage and validate the expert offsets (every CTA, so none depends on another).
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) sm.offsets[i] = p.offsets[i];
     __syncthreads();
-    if (threadIdx.x == 0) {
-      bool ok = sm.offsets[0] == 0;
-      for (int e = 0; e < p.E && ok; ++e)
-        ok = sm.offsets[e + 1] >= sm.offsets[e] && (sm.offsets[e + 1] % kBM) == 0;
-      ok = ok && sm.offsets[p.E] <= p.M;
-      if (!ok) {
-        sm.bad_offsets = 1;
-        if (blockIdx.x == 0) atomicOr(&g_device_error, kDevErrBadOffsets);
-      } else {
-        sm.rows_valid = sm.offsets[p.E];
+    if (warp == 0) {
+      // Validate, and scan the per-expert tile counts into tile_base: each
+      // lane takes a contiguous chunk of experts, then a warp prefix sum.
+      const int chunk = (p.E + 31) / 32;
+      const int e0 = lane * chunk < p.E ? lane * chunk : p.E;
+      const int e1 = e0 + chunk < p.E ? e0 + chunk : p.E;
+      bool ok = true;
+      int count = 0;
+      for (int e = e0; e < e1; ++e) {
+        const int rows = sm.offsets[e + 1] - sm.offsets[e];
+        ok = ok && rows >= 0 && (sm.offsets[e + 1] % kBM) == 0;
+        count += (rows / kBM) * p.num_n_tiles;
       }
+      ok = __all_sync(0xffffffffu, ok) && sm.offsets[0] == 0 && sm.offsets[p.E] <= p.M;
+      int incl = count;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - count;
+      for (int e = e0; e < e1; ++e) {
+        sm.tile_base[e] = run;
+        run += ((sm.offsets[e + 1] - sm.offsets[e]) / kBM) * p.num_n_tiles;
+      }
+      if (lane == 31) sm.tile_base[p.E] = incl;
+      if (lane == 0) {
+        if (!ok) {
+          sm.bad_offsets = 1;
+          if (blockIdx.x == 0) atomicOr(&g_device_error, kDevErrBadOffsets);
+        }
+      }
+      if (lane == 31) sm.num_tiles = ok ? incl : 0;
     }
   }
   if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -205,6 +230,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = sm.tmem_base;
   const bool skip_all = kGrouped && sm.bad_offsets;
+  // (re-read per tile rather than held in a register: the promotion warps
+  // have none to spare)
+#define FP8BS_NUM_TILES (kGrouped ? sm.num_tiles : p.num_m_tiles * p.num_n_tiles)
 
   if (warp < 4) {
     regs_dealloc<kProducerRegs>();
@@ -214,9 +242,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, parity_mask = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; t < FP8BS_NUM_TILES; t += gridDim.x) {
       const TileCoord tc = tile_coord<kGrouped>(t, p, sm);
-      if (!tc.valid) continue;
       for (int kb = 0; kb < p.KB; ++kb) {
         if (!bounded_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) goto producer_done;
         mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
@@ -243,9 +270,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int stage = 0, buf = 0;
     uint32_t phase = 0, tphase = 0;
     bool issued = false;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; t < FP8BS_NUM_TILES; t += gridDim.x) {
       const TileCoord tc = tile_coord<kGrouped>(t, p, sm);
-      if (!tc.valid) continue;
       for (int kb = 0; kb < p.KB; ++kb) {
         if (!bounded_wait(&sm.full[stage], phase, abort_flag)) goto mma_done;
         if (!bounded_wait(&sm.tempty[buf], tphase ^ 1u, abort_flag)) goto mma_done;
@@ -284,9 +310,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int h = (warp - 4) >> 2;   // column half (0: 0..127, 1: 128..255)
     int buf = 0;
     uint32_t tphase = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; t < FP8BS_NUM_TILES; t += gridDim.x) {
       const TileCoord tc = tile_coord<kGrouped>(t, p, sm);
-      if (!tc.valid) continue;
       const int row = tc.m0 + g * 32 + lane;
       const bool row_ok = row < p.M;
       const int col0 = tc.n0 + h * 128;
@@ -411,6 +436,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_dealloc(tmem_base, kTmemCols);
   }
 }
+
+#undef FP8BS_NUM_TILES
 
 // One CTA waits on a barrier that nothing arrives at, with a time limit; the
 // wait gives up, records a timeout in the device error word and returns.

@@ -19,6 +19,9 @@ __device__ uint32_t g_device_error = 0;
 #define FP8BS_SPIN_LIMIT_NS (1ull << 30)   // ~1.07 s: far above any legal wait
 #endif
 constexpr uint64_t kSpinLimitNs = FP8BS_SPIN_LIMIT_NS;
+// The same limit for the hot-path waits, in SM cycles: 2^31 cycles is ~1.06 s
+// at the 2032 MHz maximum clock (longer at lower clocks).
+constexpr long long kSpinLimitCycles = 1ll << 31;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -65,15 +68,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait until the phase with the given parity has completed.  Returns false if
 // the CTA's abort flag was raised (by this or another warp) or the time limit
 // ran out; in the latter case the device error word records a timeout.
+// The limit is counted in SM clock cycles (clock64 is read from a register
+// of the SM; reading %globaltimer in this loop delayed the other warps of the
+// same SM sub-partition by hundreds of cycles per wait).
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity,
                                              volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 31u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kSpinLimitNs) {
+      if (clock64() - t0 > kSpinLimitCycles) {
         atomicOr(&g_device_error, kDevErrTimeout);
         *abort_flag = 1;
         return false;
