@@ -12,6 +12,7 @@
 
 #include "../../include/fp8bs.h"
 #include "gemm_kernel.cuh"
+#include "gemm_pair_kernel.cuh"
 #include "quant_kernels.cuh"
 
 namespace fp8bs {
@@ -22,6 +23,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool init = false;
   int num_sms = 0;
+  int pair_clusters = 0;   // co-resident 2-CTA clusters of the pair GEMM
 };
 
 std::mutex g_mutex;
@@ -40,6 +42,33 @@ fp8bs_status device_info(DeviceInfo* out) {
   }
   *out = d;
   return FP8BS_OK;
+}
+
+// How many 2-CTA clusters of `kernel` fit on the device at once (queried once
+// per device; all pair-kernel variants have the same shape and resources).
+template <typename K>
+int pair_clusters(K kernel) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (d.pair_clusters == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 512, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPairSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) return 0;
+    d.pair_clusters = n;
+  }
+  return d.pair_clusters;
 }
 
 fp8bs_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
@@ -101,6 +130,25 @@ fp8bs_status make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint6
   return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
 }
 
+// Output map of the pair GEMM's TMA-store epilogue: [rows][ldc] of fp32 or
+// bf16, box = 64 bytes x 32 rows with the 64-byte swizzle.
+fp8bs_status make_map_out(CUtensorMap* m, void* base, fp8bs_dtype ct, uint64_t cols,
+                          uint64_t rows, uint64_t ld_elems) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  fp8bs_status st = encode_fn(&enc);
+  if (st != FP8BS_OK) return st;
+  const uint64_t esz = dtype_size(ct);
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld_elems * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / esz), 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, ct == FP8BS_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
 // Shared checks of the dense and grouped GEMM (all on the host, before any launch).
 fp8bs_status check_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
                         const float* sa, int64_t ldsa, const uint8_t* B, int64_t ldb,
@@ -130,6 +178,33 @@ fp8bs_status check_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
   if (sb_mode == FP8BS_SB_PERCOL && (!aligned(sb, 16) || ldsb % 4 != 0))
     return FP8BS_ERR_MISALIGNED;
   return FP8BS_OK;
+}
+
+// Launch of the CTA-pair GEMM: a persistent grid of as many 2-CTA clusters
+// as can be resident at once (at most one per tile).
+fp8bs_status launch_gemm_pair(GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                              const CUtensorMap& tc, int sb_kind, fp8bs_dtype ct,
+                              cudaStream_t stream) {
+  DeviceInfo di;
+  fp8bs_status st = device_info(&di);
+  if (st != FP8BS_OK) return st;
+  auto run = [&](auto kernel) -> fp8bs_status {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPairSmemBytes)) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
+    int clusters = pair_clusters(kernel);
+    if (clusters <= 0) return FP8BS_ERR_CUDA;
+    const int tiles = p.num_m_tiles * p.num_n_tiles;
+    if (tiles < clusters) clusters = tiles;
+    kernel<<<2 * clusters, kGemmThreads, kPairSmemBytes, stream>>>(p, ta, tb, tc);
+    return launch_status();
+  };
+  const bool bf16 = ct == FP8BS_BF16;
+  if (sb_kind == kSbBlock)
+    return bf16 ? run(fp8bs_gemm_pair_kernel<kSbBlock, true>)
+                : run(fp8bs_gemm_pair_kernel<kSbBlock, false>);
+  return bf16 ? run(fp8bs_gemm_pair_kernel<kSbPerCol, true>)
+              : run(fp8bs_gemm_pair_kernel<kSbPerCol, false>);
 }
 
 template <bool kGrouped>
@@ -310,14 +385,15 @@ fp8bs_status fp8bs_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
   fp8bs_status st = check_gemm(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc);
   if (st != FP8BS_OK || M == 0 || N == 0) return st;
   if (K == 0) return zero_fill(C, ct, M, N, ldc, as_stream(stream));
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if ((st = make_map_2d(&ta, A, K, M, lda, kBM)) != FP8BS_OK) return st;
-  if ((st = make_map_3d(&tb, B, K, N, 1, ldb, kBN)) != FP8BS_OK) return st;
+  if ((st = make_map_2d(&tb, B, K, N, ldb, kBN / 2)) != FP8BS_OK) return st;
+  if ((st = make_map_out(&tc, C, ct, N, M, ldc)) != FP8BS_OK) return st;
   GemmParams p{};
   p.M = static_cast<int32_t>(M);
   p.N = static_cast<int32_t>(N);
   p.KB = static_cast<int32_t>(K / kBK);
-  p.num_m_tiles = static_cast<int32_t>((M + kBM - 1) / kBM);
+  p.num_m_tiles = static_cast<int32_t>((M + kPairTileM - 1) / kPairTileM);
   p.num_n_tiles = static_cast<int32_t>((N + kBN - 1) / kBN);
   p.E = 1;
   p.sa = sa;
@@ -328,8 +404,8 @@ fp8bs_status fp8bs_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
   p.C = C;
   p.ldc = ldc;
   p.offsets = nullptr;
-  return launch_gemm<false>(p, ta, tb, sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct,
-                            as_stream(stream));
+  return launch_gemm_pair(p, ta, tb, tc, sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct,
+                          as_stream(stream));
 }
 
 fp8bs_status fp8bs_grouped_gemm(int32_t E, const int32_t* offsets, int64_t M_cap, int64_t N,

@@ -1,0 +1,334 @@
+// Block-scaled FP8 GEMM on CTA pairs (tcgen05 cta_group::2): the dense path of
+// fp8bs_gemm.
+//
+// Same method as gemm_kernel.cuh ("Should Fixing Deepseek Take 60 Steps?",
+// Figure 6 and Figure 7 (a) passages; untitled page at jp-study.kr, Figure 7 (b)
+// passage): every 128-deep K-slab is multiplied on the tensor cores and its
+// partial sum is promoted into FP32 registers on CUDA cores with the row scale
+// and the column-block (or column) scale of that slab.
+//
+// Why pairs: with one CTA per 128x256 tile each SM pulls 48 KB of operands per
+// slab from L2 and only four such stages fit in shared memory; measured, the
+// TMA round trip (~2900 cycles at that load) then bounds the slab rate.  A
+// cluster of two CTAs computes a 256x256 tile with one pair MMA: each CTA
+// stages its own 128 rows of A and one half (128 rows) of B, so an SM pulls
+// 32 KB per slab and six stages fit.
+//
+// Roles (384 threads per CTA, both CTAs of the pair):
+//   warp 0      TMA producer: this CTA's A rows and B half of each slab; the
+//               loads complete on the even CTA's `full` barrier.
+//   warp 1      even CTA only: issues 4 x tcgen05.mma.cta_group::2 (M=256,
+//               N=256, K=32) per slab into one of two 256-column TMEM buffers,
+//               then one commit that arrives on `done[stage]` in both CTAs:
+//               the stage may be refilled and the TMEM slab may be read.
+//   warps 4..11 promotion + epilogue of this CTA's 128 rows (as in the
+//               single-CTA kernel); each warp releases its TMEM columns by
+//               arriving on the even CTA's `tmem_free` barrier (16 arrivals).
+//               The epilogue goes out through TMA stores: each warp writes a
+//               32-row x 64-byte chunk of its rows into a 2 KB shared buffer
+//               (64-byte swizzle, conflict-free) and one lane stores the box.
+//               (Stores straight from registers, one row per lane, hit 32
+//               cache lines per instruction: ~13k cycles per FP32 tile.)
+#pragma once
+#include "gemm_kernel.cuh"
+
+namespace fp8bs {
+
+constexpr int kPairStages = 6;
+constexpr int kPairStageA = kBM * kBK;          // this CTA's 128 rows of A, one slab
+constexpr int kPairStageB = (kBN / 2) * kBK;    // this CTA's half of the B tile
+constexpr int kPairStageBytes = kPairStageA + kPairStageB;
+constexpr int kPairTileM = 2 * kBM;             // rows of a pair tile
+
+constexpr int kEpiStageBytes = 32 * 64;       // one warp's output chunk: 32 rows x 64 B
+
+struct PairSmem {
+  alignas(1024) unsigned char epi_stage[kEpiWarps][kEpiStageBytes];
+  uint64_t full[kPairStages];   // even CTA: both CTAs' loads of a slab have landed
+  uint64_t done[kPairStages];   // both CTAs: the slab's MMAs are complete
+  uint64_t tmem_free[2];        // even CTA: 16 promotion warps released a TMEM buffer
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  alignas(16) float sb_stage[kEpiWarps][2][128];
+};
+
+constexpr size_t kPairSmemBytes =
+    1024 /* alignment slack */ + static_cast<size_t>(kPairStages) * kPairStageBytes +
+    sizeof(PairSmem);
+
+// p.num_m_tiles counts 256-row pair tiles here.
+template <int kSb, bool kOutBf16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    fp8bs_gemm_pair_kernel(const __grid_constant__ GemmParams p,
+                           const __grid_constant__ CUtensorMap tmap_a,
+                           const __grid_constant__ CUtensorMap tmap_b,
+                           const __grid_constant__ CUtensorMap tmap_c) {
+  extern __shared__ __align__(1024) unsigned char pair_smem_raw[];
+  const uint32_t raw_addr = smem_u32(pair_smem_raw);
+  unsigned char* ring = pair_smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  PairSmem& sm =
+      *reinterpret_cast<PairSmem*>(ring + static_cast<size_t>(kPairStages) * kPairStageBytes);
+  const uint32_t ring_addr = smem_u32(ring);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0: the CTA that issues the MMAs
+  // (tile bounds and strides are recomputed from the parameters and special
+  // registers rather than held: the promotion warps have no registers to spare)
+#define PAIR_FIRST static_cast<int>(blockIdx.x >> 1)
+#define PAIR_STRIDE static_cast<int>(gridDim.x >> 1)
+#define PAIR_TILES (p.num_m_tiles * p.num_n_tiles)
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.done[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) mbar_init(&sm.tmem_free[b], 2 * kEpiWarps);
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+    tma_prefetch_desc(&tmap_c);
+  }
+  if (warp == 1) tmem_alloc_pair(&sm.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync();   // barriers of both CTAs initialised, TMEM allocated in both
+  tc_fence_after();
+  const uint32_t tmem_base = sm.tmem_base;
+
+  if (warp < 4) {
+    regs_dealloc<kProducerRegs>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------------- TMA
+      // A rows are re-read by every wave of the m-fastest walk (keep them in
+      // L2); a B panel is consumed by the CTAs of one wave (measured: Fprop
+      // 0.488 -> 0.438 ms against evict_last for both).
+      const uint64_t policy_a = l2_policy_evict_last();
+      const uint64_t policy_b = l2_policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, parity_mask = 0;
+      bool aborted = false;
+      for (int t = PAIR_FIRST; t < PAIR_TILES && !aborted; t += PAIR_STRIDE) {
+        const int a_row = (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM;
+        const int b_row = (t / p.num_m_tiles) * kBN + static_cast<int>(rank) * (kBN / 2);
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!bounded_wait(&sm.done[stage], phase ^ 1u, abort_flag)) {
+            aborted = true;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(&sm.full[stage], 2 * kPairStageBytes);
+          const uint32_t full_bar = mapa_shared(smem_u32(&sm.full[stage]), 0);
+          const uint32_t dst = ring_addr + stage * kPairStageBytes;
+          tma_load_2d_pair(dst, &tmap_a, kb * kBK, a_row, full_bar, policy_a);
+          tma_load_2d_pair(dst + kPairStageA, &tmap_b, kb * kBK, b_row, full_bar, policy_b);
+          issued_mask |= 1u << stage;
+          parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every load issued must land before either CTA may exit.  The even CTA
+      // sees both CTAs' bytes on its `full` barriers; the odd CTA cannot wait
+      // on them, so after an abort it gives its own copies time to land.
+      if (rank == 0) {
+        for (int s = 0; s < kPairStages; ++s)
+          if (issued_mask & (1u << s))
+            bounded_wait_noabort(&sm.full[s], (parity_mask >> s) & 1u, kSpinLimitNs);
+      } else if (aborted) {
+        __nanosleep(100000);
+      }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+      // ---------------------------------------------------------------- MMA
+      constexpr uint32_t idesc = idesc_e4m3_f32(kPairTileM, kBN);
+      int stage = 0, buf = 0;
+      uint32_t phase = 0, tphase = 0;
+      bool issued = false;
+      for (int t = PAIR_FIRST; t < PAIR_TILES; t += PAIR_STRIDE) {
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!bounded_wait(&sm.full[stage], phase, abort_flag)) goto mma_done;
+          if (!bounded_wait(&sm.tmem_free[buf], tphase ^ 1u, abort_flag)) goto mma_done;
+          tc_fence_after();
+          const uint32_t a_addr = ring_addr + stage * kPairStageBytes;
+          const uint64_t adesc = smem_desc_k_sw128(a_addr);
+          const uint64_t bdesc = smem_desc_k_sw128(a_addr + kPairStageA);
+          const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)  // 32 bytes = 32 E4M3 values per MMA
+            mma_f8f6f4_pair(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+          mma_commit_pair(&sm.done[stage], 0x3);
+          issued = true;
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++buf == 2) {
+            buf = 0;
+            tphase ^= 1u;
+          }
+        }
+      }
+    mma_done:
+      if (issued) {  // all MMAs must finish before TMEM is released in either CTA
+        mma_commit_pair(&sm.drain, 0x1);
+        bounded_wait_noabort(&sm.drain, 0, kSpinLimitNs);
+      }
+    }
+  } else {
+    regs_alloc<kEpilogueRegs>();
+    // ------------------------------------------------- promotion + epilogue
+    const int g = warp & 3;          // TMEM lane group (rows 32g .. 32g+31 of this CTA)
+    const int h = (warp - 4) >> 2;   // column half (0: 0..127, 1: 128..255)
+    int buf = 0, stage = 0;
+    uint32_t phase = 0;
+    for (int t = PAIR_FIRST; t < PAIR_TILES; t += PAIR_STRIDE) {
+      const int row = (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM + g * 32 + lane;
+      const bool row_ok = row < p.M;
+      const int col0 = (t / p.num_m_tiles) * kBN + h * 128;
+      const bool cols_ok = col0 < p.N;
+      float2 acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
+
+      auto load_sa = [&](int kb) -> float {
+        return (row_ok && kb < p.KB) ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ldsa + row)
+                                     : 0.0f;
+      };
+      auto load_sb = [&](int kb) -> float {
+        if constexpr (kSb == kSbBlock) {
+          return (cols_ok && kb < p.KB)
+                     ? __ldg(p.sb + static_cast<int64_t>(kb) * p.sb_k_stride +
+                             static_cast<int64_t>(col0 / 128) * p.sb_n_stride)
+                     : 0.0f;
+        } else {
+          return 0.0f;
+        }
+      };
+      float sa_cur = load_sa(0), sb_cur = load_sb(0);
+      // per-column mode: this warp's 128 B scales of a slab, staged in smem
+      float* sb_mine = &sm.sb_stage[warp - 4][0][0];
+      auto fetch_sb_cols = [&](int kb) -> float4 {
+        const int c = col0 + lane * 4;
+        return (kb < p.KB && c < p.N)
+                   ? __ldg(reinterpret_cast<const float4*>(p.sb + static_cast<int64_t>(kb) * p.ldsb + c))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      };
+      if constexpr (kSb == kSbPerCol) {
+        const float4 v = fetch_sb_cols(0);
+        reinterpret_cast<float4*>(sb_mine)[lane] = v;
+        __syncwarp();
+      }
+      for (int kb = 0; kb < p.KB; ++kb) {
+        const float sa_nxt = load_sa(kb + 1), sb_nxt = load_sb(kb + 1);
+        float4 sbc_nxt;
+        if constexpr (kSb == kSbPerCol) sbc_nxt = fetch_sb_cols(kb + 1);
+        if (!bounded_wait(&sm.done[stage], phase, abort_flag)) goto epilogue_done;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) +
+                               static_cast<uint32_t>(buf * kBN + h * 128);
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr, ra);
+        tmem_wait_ld(ra);
+        if constexpr (kSb == kSbBlock) {
+          const float sc = sa_cur * sb_cur;
+          const float2 sc2 = make_float2(sc, sc);
+#pragma unroll
+          for (int c = 0; c < 4; c += 2) {
+            tmem_ld32(taddr + (c + 1) * 32, rb);
+            promote32(acc + c * 16, ra, sc2);
+            tmem_wait_ld(rb);
+            if (c + 2 < 4) tmem_ld32(taddr + (c + 2) * 32, ra);
+            promote32(acc + (c + 1) * 16, rb, sc2);
+            if (c + 2 < 4) tmem_wait_ld(ra);
+          }
+        } else {
+          // columns past N carry zero scales (and zero products), so no guard is needed
+          const float2 sa2 = make_float2(sa_cur, sa_cur);
+          const float* sbs = sb_mine + (kb & 1) * 128;
+#pragma unroll
+          for (int c = 0; c < 4; c += 2) {
+            tmem_ld32(taddr + (c + 1) * 32, rb);
+            promote32_percol(acc + c * 16, ra, sbs + c * 32, sa2);
+            tmem_wait_ld(rb);
+            if (c + 2 < 4) tmem_ld32(taddr + (c + 2) * 32, ra);
+            promote32_percol(acc + (c + 1) * 16, rb, sbs + (c + 1) * 32, sa2);
+            if (c + 2 < 4) tmem_wait_ld(ra);
+          }
+          reinterpret_cast<float4*>(sb_mine + ((kb + 1) & 1) * 128)[lane] = sbc_nxt;
+          __syncwarp();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.tmem_free[buf]), 0));
+        buf ^= 1;
+        if (++stage == kPairStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        sa_cur = sa_nxt;
+        sb_cur = sb_nxt;
+      }
+      // ---- epilogue: this warp's 32 rows x 128 columns, in 64-byte-wide chunks
+      // (addresses are recomputed per store: the promotion warps have no
+      // registers to spare while the accumulators are live)
+#pragma unroll
+      for (int c = 0; c < 128 / (kOutBf16 ? 32 : 16); ++c) {
+        constexpr int kChunkCols = kOutBf16 ? 32 : 16;   // 64 bytes of output per row
+        // the previous bulk store of this buffer must have read it
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {   // 16-byte unit j of this row's 64 bytes
+          // row `lane` at 64 * lane; 16-byte unit j at position j ^ ((lane >> 1) & 3)
+          const uint32_t dst = smem_u32(&sm.epi_stage[warp - 4][0]) +
+                               static_cast<uint32_t>(lane) * 64u +
+                               ((static_cast<uint32_t>(j) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u)) << 4);
+          if constexpr (kOutBf16) {
+            const int k = c * 16 + 4 * j;   // float2 index of column c*32 + 8j
+            st_shared_v4(dst, make_uint4(pack_bf16x2(acc[k].x, acc[k].y),
+                                         pack_bf16x2(acc[k + 1].x, acc[k + 1].y),
+                                         pack_bf16x2(acc[k + 2].x, acc[k + 2].y),
+                                         pack_bf16x2(acc[k + 3].x, acc[k + 3].y)));
+          } else {
+            // two 8-byte stores straight from the accumulator register pairs
+            const int k = c * 8 + 2 * j;    // float2 index of column c*16 + 4j
+            st_shared_v2f(dst, acc[k]);
+            st_shared_v2f(dst + 8, acc[k + 1]);
+          }
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_c, col0 + c * kChunkCols,
+                       (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM + g * 32,
+                       smem_u32(&sm.epi_stage[warp - 4][0]));
+          bulk_commit_group();
+        }
+      }
+    }
+  epilogue_done:
+    if (lane == 0) bulk_wait_all();   // this warp's output stores are complete
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync();   // no CTA leaves while its peer may still touch its shared memory
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+#undef PAIR_FIRST
+#undef PAIR_STRIDE
+#undef PAIR_TILES
+
+}  // namespace fp8bs
