@@ -148,22 +148,31 @@ class LayerStep:
         self.dX = e(T, K, dt=torch.bfloat16)
         self.dW = e(K, N, dt=torch.float32)
         self.T, self.K, self.N = T, K, N
+        # one workspace for the K split of the GEMMs' last waves (the three
+        # GEMMs run in order on one stream, so they can share it)
+        self.ws_need = [fb.fp8bs_gemm_workspace_size(*s) for s in ((T, N, K), (T, K, N), (K, N, T))]
+        self.ws = e(max(self.ws_need)) if max(self.ws_need) > 0 else None
 
     def launches(self):
         fb = self.fb
         return [
             lambda s: fb.fp8bs_quant_act_1x128(self.x, self.Xq, self.Sx, s),
             lambda s: fb.fp8bs_quant_w_128x128(self.w, self.Wq, self.WqT, self.Sw, s),
-            lambda s: fb.fp8bs_gemm(self.Xq, self.Sx, self.WqT, self.Sw, fb.FP8BS_SB_BLOCK_KN,
-                                    self.Y, s),
+            lambda s: fb.fp8bs_gemm_ws(self.Xq, self.Sx, self.WqT, self.Sw, fb.FP8BS_SB_BLOCK_KN,
+                                       self.Y, self.ws, s),
             lambda s: fb.fp8bs_quant_act_1x128(self.dy, self.dYq, self.Sdy, s),
-            lambda s: fb.fp8bs_gemm(self.dYq, self.Sdy, self.Wq, self.Sw, fb.FP8BS_SB_BLOCK_NK,
-                                    self.dX, s),
+            lambda s: fb.fp8bs_gemm_ws(self.dYq, self.Sdy, self.Wq, self.Sw, fb.FP8BS_SB_BLOCK_NK,
+                                       self.dX, self.ws, s),
             lambda s: fb.fp8bs_quant_act_128x1(self.x, self.XqT, self.SxT, s),
             lambda s: fb.fp8bs_quant_act_128x1(self.dy, self.dYqT, self.SdyT, s),
-            lambda s: fb.fp8bs_gemm(self.XqT, self.SxT, self.dYqT, self.SdyT, fb.FP8BS_SB_PERCOL,
-                                    self.dW, s),
+            lambda s: fb.fp8bs_gemm_ws(self.XqT, self.SxT, self.dYqT, self.SdyT,
+                                       fb.FP8BS_SB_PERCOL, self.dW, self.ws, s),
         ]
+
+    def kernel_launches(self):
+        """Library kernels one step launches: 5 quantizers, 3 GEMMs, plus the
+        partial-sum kernel of each GEMM whose last wave is split."""
+        return 8 + sum(1 for n in self.ws_need if n > 0)
 
     def work(self):
         """(kind, algorithmic amount) per launch: bytes for quantizers, FLOPs for GEMMs."""
@@ -276,7 +285,7 @@ def run_fp8bs(args, rank, world, dist_on):
                    "l2": "inputs larger than L2 (474 MB of bf16 inputs per step)",
                    "parallelism": f"replicas x{world} (no data-path collective)"},
         "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": nk * args.steps, "clocks": clk.summary(), "extras": extras,
+        "gpu_launches": step.kernel_launches() * args.steps, "clocks": clk.summary(), "extras": extras,
     }
     return result
 
@@ -499,7 +508,10 @@ def run_case(args):
             fb.fp8bs_quant_act_128x1(dy, B, sb, stream)
             out, mode = torch.empty((K, N), dtype=torch.float32, device=dev), fb.FP8BS_SB_PERCOL
         del x, dy, w
-        fn = lambda: fb.fp8bs_gemm(A, sa, B, sb, mode, out, stream)  # noqa: E731
+        M_, K_ = A.shape
+        need = fb.fp8bs_gemm_workspace_size(M_, B.shape[0], K_)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
+        fn = lambda: fb.fp8bs_gemm_ws(A, sa, B, sb, mode, out, ws, stream)  # noqa: E731
         amount, kind = 2.0 * T * K * N, "tensor"
     elif c == "grouped":
         counts = wl.zipf_counts()

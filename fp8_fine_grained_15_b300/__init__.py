@@ -58,13 +58,16 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_gemm.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I, I64, P, I, I64, P]
         L.fp8bs_grouped_gemm.argtypes = [I32, P, I64, I64, I64, P, I64, P, I64, P, I64, P, I,
                                          I64, I64, P, I, I64, P]
+        L.fp8bs_gemm_workspace_size.argtypes = [I64, I64, I64, ctypes.POINTER(ctypes.c_size_t)]
+        L.fp8bs_gemm_ws.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I, I64, P, I, I64, P,
+                                    ctypes.c_size_t, P]
         L.fp8bs_sync_status.argtypes = [P]
         L.fp8bs_status_string.argtypes = [I]
         L.fp8bs_status_string.restype = ctypes.c_char_p
         L.fp8bs_debug_timeout_probe.argtypes = [I64, P]
         for name in ("fp8bs_quant_act_1x128", "fp8bs_quant_act_128x1", "fp8bs_quant_w_128x128",
                      "fp8bs_gemm", "fp8bs_grouped_gemm", "fp8bs_sync_status",
-                     "fp8bs_debug_timeout_probe"):
+                     "fp8bs_debug_timeout_probe", "fp8bs_gemm_workspace_size", "fp8bs_gemm_ws"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -154,6 +157,26 @@ def fp8bs_gemm(A, sa, B, sb, sb_mode: int, C, stream=None):
     _check(lib().fp8bs_gemm(M, N, K, _ptr(A), _row_stride(A), _ptr(sa), _row_stride(sa),
                             _ptr(B), _row_stride(B), _ptr(sb), sb_mode, _row_stride(sb),
                             _ptr(C), _dtype(C), _row_stride(C), _stream(stream)), "fp8bs_gemm")
+
+
+def fp8bs_gemm_workspace_size(M: int, N: int, K: int) -> int:
+    """Bytes of workspace fp8bs_gemm_ws can use for this shape (0: no split)."""
+    n = ctypes.c_size_t(0)
+    _check(lib().fp8bs_gemm_workspace_size(M, N, K, ctypes.byref(n)),
+           "fp8bs_gemm_workspace_size")
+    return n.value
+
+
+def fp8bs_gemm_ws(A, sa, B, sb, sb_mode: int, C, workspace, stream=None):
+    """fp8bs_gemm with a device workspace (uint8 tensor, or None) for the K
+    split of the last wave's tiles."""
+    M, K = A.shape
+    N = B.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fp8bs_gemm_ws(M, N, K, _ptr(A), _row_stride(A), _ptr(sa), _row_stride(sa),
+                               _ptr(B), _row_stride(B), _ptr(sb), sb_mode, _row_stride(sb),
+                               _ptr(C), _dtype(C), _row_stride(C), _ptr(workspace), ws_bytes,
+                               _stream(stream)), "fp8bs_gemm_ws")
 
 
 def fp8bs_grouped_gemm(offsets, A, sa, B, sb, sb_mode: int, C, stream=None):

@@ -182,21 +182,65 @@ fp8bs_status check_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
 
 // Launch of the CTA-pair GEMM: a persistent grid of as many 2-CTA clusters
 // as can be resident at once (at most one per tile).
+// Co-resident 2-CTA clusters of the pair GEMM on the current device (all its
+// variants have the same shape and resources).
+fp8bs_status pair_cluster_count(int* clusters) {
+  auto kernel = fp8bs_gemm_pair_kernel<kSbBlock, true>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kPairSmemBytes)) != cudaSuccess)
+    return FP8BS_ERR_CUDA;
+  *clusters = pair_clusters(kernel);
+  return *clusters > 0 ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
+// Split of the last, partial wave: its `tail` tiles are cut into `splits`
+// K-ranges so that every cluster has work; the FP32 partials need
+// tail * splits pair tiles of workspace.  ws_avail limits the split count
+// (SIZE_MAX: no limit).  No split when it would give fewer than 2 ranges.
+struct SplitPlan {
+  int full_tiles, splits, units, tail;
+  size_t ws_bytes;
+};
+constexpr int kMaxSplits = 32;
+constexpr size_t kPartialTileBytes = static_cast<size_t>(kPairTileM) * kBN * sizeof(float);
+
+SplitPlan plan_split(int tiles, int KB, int clusters, size_t ws_avail) {
+  SplitPlan sp{tiles, 1, tiles, 0, 0};
+  if (tiles <= 0 || clusters <= 0) return sp;
+  const int tail = tiles % clusters;
+  if (tail == 0) return sp;
+  int n = clusters / tail;
+  if (n > KB) n = KB;
+  if (n > kMaxSplits) n = kMaxSplits;
+  const size_t per_split = static_cast<size_t>(tail) * kPartialTileBytes;
+  if (ws_avail != SIZE_MAX && static_cast<size_t>(n) > ws_avail / per_split)
+    n = static_cast<int>(ws_avail / per_split);
+  if (n < 2) return sp;
+  sp.full_tiles = tiles - tail;
+  sp.splits = n;
+  sp.units = sp.full_tiles + tail * n;
+  sp.tail = tail;
+  sp.ws_bytes = per_split * n;
+  return sp;
+}
+
 fp8bs_status launch_gemm_pair(GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                              const CUtensorMap& tc, int sb_kind, fp8bs_dtype ct,
+                              const CUtensorMap& tc, const CUtensorMap& tws, const float* ws,
+                              int tail, int clusters, int sb_kind, fp8bs_dtype ct,
                               cudaStream_t stream) {
-  DeviceInfo di;
-  fp8bs_status st = device_info(&di);
-  if (st != FP8BS_OK) return st;
   auto run = [&](auto kernel) -> fp8bs_status {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kPairSmemBytes)) != cudaSuccess)
       return FP8BS_ERR_CUDA;
-    int clusters = pair_clusters(kernel);
-    if (clusters <= 0) return FP8BS_ERR_CUDA;
-    const int tiles = p.num_m_tiles * p.num_n_tiles;
-    if (tiles < clusters) clusters = tiles;
-    kernel<<<2 * clusters, kGemmThreads, kPairSmemBytes, stream>>>(p, ta, tb, tc);
+    const int grid_clusters = p.units < clusters ? p.units : clusters;
+    kernel<<<2 * grid_clusters, kGemmThreads, kPairSmemBytes, stream>>>(p, ta, tb, tc, tws);
+    fp8bs_status st = launch_status();
+    if (st != FP8BS_OK || tail == 0) return st;
+    const unsigned blocks = static_cast<unsigned>(tail) * (kPairTileM * 64 / 256);
+    if (ct == FP8BS_BF16)
+      split_fixup_kernel<true><<<blocks, 256, 0, stream>>>(ws, p, tail);
+    else
+      split_fixup_kernel<false><<<blocks, 256, 0, stream>>>(ws, p, tail);
     return launch_status();
   };
   const bool bf16 = ct == FP8BS_BF16;
@@ -292,6 +336,49 @@ void launch_quant_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_
       q, ldq, s, lds);
 }
 
+// Dense GEMM on CTA pairs; with a workspace, the tail tiles are split along K.
+fp8bs_status gemm_dense(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                        const float* sa, int64_t ldsa, const uint8_t* B, int64_t ldb,
+                        const float* sb, fp8bs_bscale sb_mode, int64_t ldsb, void* C,
+                        fp8bs_dtype ct, int64_t ldc, float* ws, size_t ws_bytes, void* stream) {
+  fp8bs_status st = check_gemm(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc);
+  if (st != FP8BS_OK || M == 0 || N == 0) return st;
+  if (K == 0) return zero_fill(C, ct, M, N, ldc, as_stream(stream));
+  CUtensorMap ta, tb, tc;
+  if ((st = make_map_2d(&ta, A, K, M, lda, kBM)) != FP8BS_OK) return st;
+  if ((st = make_map_2d(&tb, B, K, N, ldb, kBN / 2)) != FP8BS_OK) return st;
+  if ((st = make_map_out(&tc, C, ct, N, M, ldc)) != FP8BS_OK) return st;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(N);
+  p.KB = static_cast<int32_t>(K / kBK);
+  p.num_m_tiles = static_cast<int32_t>((M + kPairTileM - 1) / kPairTileM);
+  p.num_n_tiles = static_cast<int32_t>((N + kBN - 1) / kBN);
+  p.E = 1;
+  p.sa = sa;
+  p.ldsa = ldsa;
+  p.sb = sb;
+  fill_scale_strides(p, sb_mode, ldsb);
+  p.sb_e_stride = 0;
+  p.C = C;
+  p.ldc = ldc;
+  p.offsets = nullptr;
+  int clusters = 0;
+  if ((st = pair_cluster_count(&clusters)) != FP8BS_OK) return st;
+  const SplitPlan sp = plan_split(p.num_m_tiles * p.num_n_tiles, p.KB, clusters,
+                                  ws != nullptr ? ws_bytes : 0);
+  p.full_tiles = sp.full_tiles;
+  p.splits = sp.splits;
+  p.units = sp.units;
+  CUtensorMap tws = tc;   // unused without a split
+  if (sp.tail > 0 &&
+      (st = make_map_out(&tws, ws, FP8BS_F32, kBN,
+                         static_cast<uint64_t>(sp.tail) * sp.splits * kPairTileM, kBN)) != FP8BS_OK)
+    return st;
+  return launch_gemm_pair(p, ta, tb, tc, tws, ws, sp.tail, clusters,
+                          sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct, as_stream(stream));
+}
+
 }  // namespace
 }  // namespace fp8bs
 
@@ -382,30 +469,32 @@ fp8bs_status fp8bs_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
                         const float* sa, int64_t ldsa, const uint8_t* B, int64_t ldb,
                         const float* sb, fp8bs_bscale sb_mode, int64_t ldsb, void* C,
                         fp8bs_dtype ct, int64_t ldc, void* stream) {
-  fp8bs_status st = check_gemm(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc);
-  if (st != FP8BS_OK || M == 0 || N == 0) return st;
-  if (K == 0) return zero_fill(C, ct, M, N, ldc, as_stream(stream));
-  CUtensorMap ta, tb, tc;
-  if ((st = make_map_2d(&ta, A, K, M, lda, kBM)) != FP8BS_OK) return st;
-  if ((st = make_map_2d(&tb, B, K, N, ldb, kBN / 2)) != FP8BS_OK) return st;
-  if ((st = make_map_out(&tc, C, ct, N, M, ldc)) != FP8BS_OK) return st;
-  GemmParams p{};
-  p.M = static_cast<int32_t>(M);
-  p.N = static_cast<int32_t>(N);
-  p.KB = static_cast<int32_t>(K / kBK);
-  p.num_m_tiles = static_cast<int32_t>((M + kPairTileM - 1) / kPairTileM);
-  p.num_n_tiles = static_cast<int32_t>((N + kBN - 1) / kBN);
-  p.E = 1;
-  p.sa = sa;
-  p.ldsa = ldsa;
-  p.sb = sb;
-  fill_scale_strides(p, sb_mode, ldsb);
-  p.sb_e_stride = 0;
-  p.C = C;
-  p.ldc = ldc;
-  p.offsets = nullptr;
-  return launch_gemm_pair(p, ta, tb, tc, sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct,
-                          as_stream(stream));
+  return gemm_dense(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc, nullptr, 0,
+                    stream);
+}
+
+fp8bs_status fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
+  if (bytes == nullptr || M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (M == 0 || N == 0 || K == 0) return FP8BS_OK;
+  if (K % kBK != 0 || M > INT_MAX - kPairTileM || N > INT_MAX - kBN) return FP8BS_ERR_UNSUPPORTED;
+  int clusters = 0;
+  fp8bs_status st = pair_cluster_count(&clusters);
+  if (st != FP8BS_OK) return st;
+  const int64_t tiles = ((M + kPairTileM - 1) / kPairTileM) * ((N + kBN - 1) / kBN);
+  if (tiles > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+  *bytes = plan_split(static_cast<int>(tiles), static_cast<int>(K / kBK), clusters, SIZE_MAX).ws_bytes;
+  return FP8BS_OK;
+}
+
+fp8bs_status fp8bs_gemm_ws(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                           const float* sa, int64_t ldsa, const uint8_t* B, int64_t ldb,
+                           const float* sb, fp8bs_bscale sb_mode, int64_t ldsb, void* C,
+                           fp8bs_dtype ct, int64_t ldc, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (workspace != nullptr && !aligned(workspace, 256)) return FP8BS_ERR_MISALIGNED;
+  return gemm_dense(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc,
+                    static_cast<float*>(workspace), workspace ? workspace_bytes : 0, stream);
 }
 
 fp8bs_status fp8bs_grouped_gemm(int32_t E, const int32_t* offsets, int64_t M_cap, int64_t N,

@@ -69,6 +69,11 @@ struct GemmParams {
   void* C;
   int64_t ldc;          // elements
   const int32_t* offsets;  // grouped: device offsets[E+1]
+  // pair kernel work units: tiles [0, full_tiles) whole, then each remaining
+  // tile as `splits` K-ranges whose FP32 partials go to a workspace
+  int32_t full_tiles;
+  int32_t splits;
+  int32_t units;
 };
 
 struct GemmSmem {

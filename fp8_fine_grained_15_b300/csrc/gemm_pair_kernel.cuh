@@ -39,6 +39,13 @@ constexpr int kPairStageA = kBM * kBK;          // this CTA's 128 rows of A, one
 constexpr int kPairStageB = (kBN / 2) * kBK;    // this CTA's half of the B tile
 constexpr int kPairStageBytes = kPairStageA + kPairStageB;
 constexpr int kPairTileM = 2 * kBM;             // rows of a pair tile
+// Register split of the pair kernel: its producer warpgroup (TMA and MMA issue
+// loops) keeps 40 per thread so the promotion warpgroups can hold 232
+// (128 x 40 + 256 x 232 = 64512 = 168 x 384).
+constexpr uint32_t kPairProducerRegs = 40;
+constexpr uint32_t kPairEpilogueRegs = 232;
+static_assert(128 * kPairProducerRegs + 256 * kPairEpilogueRegs <= 168 * kGemmThreads,
+              "register split exceeds the launch budget");
 
 constexpr int kEpiStageBytes = 32 * 64;       // one warp's output chunk: 32 rows x 64 B
 
@@ -57,13 +64,111 @@ constexpr size_t kPairSmemBytes =
     1024 /* alignment slack */ + static_cast<size_t>(kPairStages) * kPairStageBytes +
     sizeof(PairSmem);
 
+// Work unit u of the persistent walk: a whole tile, or one K-range of a tail
+// tile (the tiles of the last, partial wave are split along K so that every
+// cluster has work; their FP32 partials are summed by split_fixup_kernel).
+struct PairUnit {
+  int tile, kb0, kb1;
+  int slot;   // < 0: whole tile, stored to C; else the partial's workspace slot
+};
+
+__device__ __forceinline__ PairUnit pair_unit(int u, const GemmParams& p) {
+  PairUnit w;
+  if (u < p.full_tiles) {
+    w.tile = u;
+    w.kb0 = 0;
+    w.kb1 = p.KB;
+    w.slot = -1;
+  } else {
+    const int v = u - p.full_tiles;
+    const int sp = v % p.splits;
+    w.tile = p.full_tiles + v / p.splits;
+    w.kb0 = (sp * p.KB) / p.splits;
+    w.kb1 = ((sp + 1) * p.KB) / p.splits;
+    w.slot = v;
+  }
+  return w;
+}
+
+// Store this warp's 32 rows x 128 accumulator columns (row `lane` per
+// thread) through a 2 KB shared buffer and 64-byte-wide TMA boxes at (col, row)
+// of `tmap`: FP32 (16 columns per box) or BF16 rounded to nearest even (32).
+template <bool kBf16>
+__device__ __forceinline__ void store_rows_tma(const float2* acc, uint32_t stg, int lane,
+                                               const CUtensorMap* tmap, int col, int row) {
+  constexpr int kChunkCols = kBf16 ? 32 : 16;   // 64 bytes of output per row
+#pragma unroll
+  for (int c = 0; c < 128 / kChunkCols; ++c) {
+    // the previous bulk store of this buffer must have read it
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // 16-byte unit j of this row's 64 bytes
+      // row `lane` at 64 * lane; 16-byte unit j at position j ^ ((lane >> 1) & 3)
+      const uint32_t dst = stg + static_cast<uint32_t>(lane) * 64u +
+                           ((static_cast<uint32_t>(j) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u)) << 4);
+      if constexpr (kBf16) {
+        const int k = c * 16 + 4 * j;   // float2 index of column c*32 + 8j
+        st_shared_v4(dst, make_uint4(pack_bf16x2(acc[k].x, acc[k].y),
+                                     pack_bf16x2(acc[k + 1].x, acc[k + 1].y),
+                                     pack_bf16x2(acc[k + 2].x, acc[k + 2].y),
+                                     pack_bf16x2(acc[k + 3].x, acc[k + 3].y)));
+      } else {
+        // two 8-byte stores straight from the accumulator register pairs
+        const int k = c * 8 + 2 * j;    // float2 index of column c*16 + 4j
+        st_shared_v2f(dst, acc[k]);
+        st_shared_v2f(dst + 8, acc[k + 1]);
+      }
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmap, col + c * kChunkCols, row, stg);
+      bulk_commit_group();
+    }
+  }
+}
+
+// Sum of the K-range partials of the tail tiles, in split order, converted to
+// the output type.  One thread per 4 columns of one row of one tail tile.
+template <bool kOutBf16>
+__global__ void __launch_bounds__(256) split_fixup_kernel(const float* __restrict__ ws,
+                                                          GemmParams p, int tail_tiles) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int q = static_cast<int>(idx % 64);
+  const int r = static_cast<int>((idx / 64) % kPairTileM);
+  const int64_t tt = idx / (64 * kPairTileM);
+  if (tt >= tail_tiles) return;
+  const int tile = p.full_tiles + static_cast<int>(tt);
+  const int row = (tile % p.num_m_tiles) * kPairTileM + r;
+  const int col = (tile / p.num_m_tiles) * kBN + q * 4;
+  if (row >= p.M || col >= p.N) return;   // N is a multiple of 16: col..col+3 < N
+  float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sp = 0; sp < p.splits; ++sp) {
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(
+        ws + ((tt * p.splits + sp) * kPairTileM + r) * static_cast<int64_t>(kBN) + q * 4));
+    sum.x += v.x;
+    sum.y += v.y;
+    sum.z += v.z;
+    sum.w += v.w;
+  }
+  if constexpr (kOutBf16) {
+    __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + static_cast<int64_t>(row) * p.ldc + col;
+    *reinterpret_cast<uint2*>(c) = make_uint2(pack_bf16x2(sum.x, sum.y), pack_bf16x2(sum.z, sum.w));
+  } else {
+    float* c = reinterpret_cast<float*>(p.C) + static_cast<int64_t>(row) * p.ldc + col;
+    *reinterpret_cast<float4*>(c) = sum;
+  }
+}
+
 // p.num_m_tiles counts 256-row pair tiles here.
 template <int kSb, bool kOutBf16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     fp8bs_gemm_pair_kernel(const __grid_constant__ GemmParams p,
                            const __grid_constant__ CUtensorMap tmap_a,
                            const __grid_constant__ CUtensorMap tmap_b,
-                           const __grid_constant__ CUtensorMap tmap_c) {
+                           const __grid_constant__ CUtensorMap tmap_c,
+                           const __grid_constant__ CUtensorMap tmap_ws) {
   extern __shared__ __align__(1024) unsigned char pair_smem_raw[];
   const uint32_t raw_addr = smem_u32(pair_smem_raw);
   unsigned char* ring = pair_smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -78,7 +183,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   // registers rather than held: the promotion warps have no registers to spare)
 #define PAIR_FIRST static_cast<int>(blockIdx.x >> 1)
 #define PAIR_STRIDE static_cast<int>(gridDim.x >> 1)
-#define PAIR_TILES (p.num_m_tiles * p.num_n_tiles)
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -102,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = sm.tmem_base;
 
   if (warp < 4) {
-    regs_dealloc<kProducerRegs>();
+    regs_dealloc<kPairProducerRegs>();
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------------- TMA
       // A rows are re-read by every wave of the m-fastest walk (keep them in
@@ -114,10 +218,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, parity_mask = 0;
       bool aborted = false;
-      for (int t = PAIR_FIRST; t < PAIR_TILES && !aborted; t += PAIR_STRIDE) {
-        const int a_row = (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM;
-        const int b_row = (t / p.num_m_tiles) * kBN + static_cast<int>(rank) * (kBN / 2);
-        for (int kb = 0; kb < p.KB; ++kb) {
+      for (int u = PAIR_FIRST; u < p.units && !aborted; u += PAIR_STRIDE) {
+        const PairUnit w = pair_unit(u, p);
+        const int a_row = (w.tile % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM;
+        const int b_row = (w.tile / p.num_m_tiles) * kBN + static_cast<int>(rank) * (kBN / 2);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!bounded_wait(&sm.done[stage], phase ^ 1u, abort_flag)) {
             aborted = true;
             break;
@@ -151,8 +256,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       int stage = 0, buf = 0;
       uint32_t phase = 0, tphase = 0;
       bool issued = false;
-      for (int t = PAIR_FIRST; t < PAIR_TILES; t += PAIR_STRIDE) {
-        for (int kb = 0; kb < p.KB; ++kb) {
+      for (int u = PAIR_FIRST; u < p.units; u += PAIR_STRIDE) {
+        const PairUnit w = pair_unit(u, p);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!bounded_wait(&sm.full[stage], phase, abort_flag)) goto mma_done;
           if (!bounded_wait(&sm.tmem_free[buf], tphase ^ 1u, abort_flag)) goto mma_done;
           tc_fence_after();
@@ -182,13 +288,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
-    regs_alloc<kEpilogueRegs>();
+    regs_alloc<kPairEpilogueRegs>();
     // ------------------------------------------------- promotion + epilogue
     const int g = warp & 3;          // TMEM lane group (rows 32g .. 32g+31 of this CTA)
     const int h = (warp - 4) >> 2;   // column half (0: 0..127, 1: 128..255)
     int buf = 0, stage = 0;
     uint32_t phase = 0;
-    for (int t = PAIR_FIRST; t < PAIR_TILES; t += PAIR_STRIDE) {
+    for (int u = PAIR_FIRST; u < p.units; u += PAIR_STRIDE) {
+      const PairUnit w = pair_unit(u, p);
+      const int t = w.tile;
       const int row = (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM + g * 32 + lane;
       const bool row_ok = row < p.M;
       const int col0 = (t / p.num_m_tiles) * kBN + h * 128;
@@ -211,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           return 0.0f;
         }
       };
-      float sa_cur = load_sa(0), sb_cur = load_sb(0);
+      float sa_cur = load_sa(w.kb0), sb_cur = load_sb(w.kb0);
       // per-column mode: this warp's 128 B scales of a slab, staged in smem
       float* sb_mine = &sm.sb_stage[warp - 4][0][0];
       auto fetch_sb_cols = [&](int kb) -> float4 {
@@ -221,11 +329,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
       };
       if constexpr (kSb == kSbPerCol) {
-        const float4 v = fetch_sb_cols(0);
-        reinterpret_cast<float4*>(sb_mine)[lane] = v;
+        const float4 v = fetch_sb_cols(w.kb0);
+        reinterpret_cast<float4*>(sb_mine + (w.kb0 & 1) * 128)[lane] = v;
         __syncwarp();
       }
-      for (int kb = 0; kb < p.KB; ++kb) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
         const float sa_nxt = load_sa(kb + 1), sb_nxt = load_sb(kb + 1);
         float4 sbc_nxt;
         if constexpr (kSb == kSbPerCol) sbc_nxt = fetch_sb_cols(kb + 1);
@@ -275,42 +383,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         sa_cur = sa_nxt;
         sb_cur = sb_nxt;
       }
-      // ---- epilogue: this warp's 32 rows x 128 columns, in 64-byte-wide chunks
-      // (addresses are recomputed per store: the promotion warps have no
+      // ---- epilogue: this warp's 32 rows x 128 columns, through TMA stores
+      // (addresses are recomputed, not held: the promotion warps have no
       // registers to spare while the accumulators are live)
-#pragma unroll
-      for (int c = 0; c < 128 / (kOutBf16 ? 32 : 16); ++c) {
-        constexpr int kChunkCols = kOutBf16 ? 32 : 16;   // 64 bytes of output per row
-        // the previous bulk store of this buffer must have read it
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {   // 16-byte unit j of this row's 64 bytes
-          // row `lane` at 64 * lane; 16-byte unit j at position j ^ ((lane >> 1) & 3)
-          const uint32_t dst = smem_u32(&sm.epi_stage[warp - 4][0]) +
-                               static_cast<uint32_t>(lane) * 64u +
-                               ((static_cast<uint32_t>(j) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u)) << 4);
-          if constexpr (kOutBf16) {
-            const int k = c * 16 + 4 * j;   // float2 index of column c*32 + 8j
-            st_shared_v4(dst, make_uint4(pack_bf16x2(acc[k].x, acc[k].y),
-                                         pack_bf16x2(acc[k + 1].x, acc[k + 1].y),
-                                         pack_bf16x2(acc[k + 2].x, acc[k + 2].y),
-                                         pack_bf16x2(acc[k + 3].x, acc[k + 3].y)));
-          } else {
-            // two 8-byte stores straight from the accumulator register pairs
-            const int k = c * 8 + 2 * j;    // float2 index of column c*16 + 4j
-            st_shared_v2f(dst, acc[k]);
-            st_shared_v2f(dst + 8, acc[k + 1]);
-          }
-        }
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmap_c, col0 + c * kChunkCols,
-                       (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM + g * 32,
-                       smem_u32(&sm.epi_stage[warp - 4][0]));
-          bulk_commit_group();
-        }
+      if (w.slot < 0) {
+        store_rows_tma<kOutBf16>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_c, col0,
+                                 (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM + g * 32);
+      } else {
+        store_rows_tma<false>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_ws, h * 128,
+                              w.slot * kPairTileM + static_cast<int>(rank) * kBM + g * 32);
       }
     }
   epilogue_done:
@@ -329,6 +410,5 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 
 #undef PAIR_FIRST
 #undef PAIR_STRIDE
-#undef PAIR_TILES
 
 }  // namespace fp8bs

@@ -47,6 +47,7 @@
 #ifndef FP8BS_H
 #define FP8BS_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -124,7 +125,7 @@ fp8bs_status fp8bs_quant_w_128x128(const void* w, fp8bs_dtype wt, int64_t R, int
  * Fprop  : A = Xq (1x128), B = WqT, sb = Sw as BLOCK_KN, C bf16.
  * Dgrad  : A = dYq (1x128), B = Wq, sb = Sw as BLOCK_NK, C bf16.
  * Wgrad  : A = XqT (128x1), B = dYqT (128x1), sb = S_dY as PERCOL, C fp32.
- * Requirements: K % 128 == 0; N % 128 == 0 for BLOCK modes, N % 8 == 0 for
+ * Requirements: K % 128 == 0; N % 128 == 0 for BLOCK modes, N % 16 == 0 for
  * PERCOL (UNSUPPORTED); A, B, C 16-byte aligned; lda, ldb, ldc*sizeof(ct)
  * multiples of 16 (MISALIGNED); sa, sb 4-byte aligned.  M, N == 0: no-op;
  * K == 0 writes zeros.  Any M >= 1 is allowed (the last row tile is ragged). */
@@ -132,6 +133,32 @@ fp8bs_status fp8bs_gemm(int64_t M, int64_t N, int64_t K,
                         const uint8_t* A, int64_t lda, const float* sa, int64_t ldsa,
                         const uint8_t* B, int64_t ldb, const float* sb, fp8bs_bscale sb_mode,
                         int64_t ldsb, void* C, fp8bs_dtype ct, int64_t ldc, void* stream);
+
+/* Bytes of workspace fp8bs_gemm_ws can use for an M x N x K GEMM on the
+ * current device (0: this shape runs no split).  The dense GEMM walks its
+ * 256 x 256 output tiles persistently over the device's CTA pairs; when the
+ * last wave is partial, its tiles can be split along K over the idle pairs,
+ * each K-range leaving a 256 x 256 FP32 partial in the workspace.
+ * Requirements: bytes non-NULL (INVALID_ARG); K % 128 == 0 (UNSUPPORTED). */
+fp8bs_status fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+
+/* fp8bs_gemm with a device workspace for the split of the last wave (above):
+ * the partials go to the workspace and a second kernel on the same stream adds
+ * them in K order (deterministic: repeated calls give identical bits) and
+ * writes C.  The tail tiles are summed in a different order than in
+ * fp8bs_gemm, so the two agree within the GEMM tolerance, not bit for bit.
+ *   workspace        device memory owned by the caller, 256-byte aligned
+ *                    (MISALIGNED otherwise), or NULL (no split);
+ *   workspace_bytes  its size; fewer K-ranges are used when it holds less than
+ *                    fp8bs_gemm_workspace_size, and no split below two.
+ * The workspace is written before it is read; its contents afterwards are
+ * undefined.  Calls that share a workspace must be ordered (one stream).
+ * All other arguments, requirements and errors are those of fp8bs_gemm. */
+fp8bs_status fp8bs_gemm_ws(int64_t M, int64_t N, int64_t K,
+                           const uint8_t* A, int64_t lda, const float* sa, int64_t ldsa,
+                           const uint8_t* B, int64_t ldb, const float* sb, fp8bs_bscale sb_mode,
+                           int64_t ldsb, void* C, fp8bs_dtype ct, int64_t ldc, void* workspace,
+                           size_t workspace_bytes, void* stream);
 
 /* Grouped block-scaled FP8 GEMM for MoE experts: expert e owns rows
  * offsets[e] .. offsets[e+1]-1 of A and C and multiplies them by B[e]:

@@ -6,6 +6,8 @@ import numpy as np
 import torch
 
 import fp8_fine_grained_15_b300 as fb
+import oracle
+import workloads as wl
 from workloads import bf16_bits
 
 DEV = "cuda:0"
@@ -86,3 +88,35 @@ def assert_gemm_close(c_gpu, c_ref, s_abs, bf16_out: bool, what: str = ""):
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; "
                              f"first (index, gpu, ref, bound): {detail}")
     return float(np.max(err / np.maximum(bound, 1e-300)))
+
+
+MODES = {"KN": oracle.SB_BLOCK_KN, "NK": oracle.SB_BLOCK_NK, "PERCOL": oracle.SB_PERCOL}
+
+
+def gemm_operands(M, N, K, mode, seed):
+    """Oracle-quantized A [M x K] (1x128) and B [N x K] with scales in `mode` layout."""
+    a = wl.random_matrix((M, K), seed=seed, dtype=torch.bfloat16)
+    Aq, sa = oracle.quant_act_1x128(oracle_input(a))
+    if mode == "PERCOL":
+        bt = wl.random_matrix((K, N), seed=seed + 1, dtype=torch.bfloat16, std=1e-3)
+        Bq, sb = oracle.quant_act_128x1(oracle_input(bt))       # [N x K], [K/128 x N]
+    else:
+        w = wl.random_matrix((K, N), seed=seed + 1, dtype=torch.bfloat16, std=0.02)
+        Wq, WqT, sw = oracle.quant_w_128x128(oracle_input(w))   # sw [K/128 x N/128]
+        Bq, sb = WqT, sw
+        if mode == "NK":
+            sb = np.ascontiguousarray(sw.T)                      # [N/128 x K/128]
+    return Aq, sa, Bq, sb
+
+
+def gpu_gemm_ws(A, sa, B, sb, sb_mode, out_dtype=torch.bfloat16, ws_bytes=None):
+    """fp8bs_gemm_ws with a workspace of ws_bytes (default: the full size the
+    library asks for; 0: no workspace)."""
+    M, N = A.shape[0], B.shape[0]
+    if ws_bytes is None:
+        ws_bytes = fb.fp8bs_gemm_workspace_size(M, N, A.shape[1])
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV) if ws_bytes > 0 else None
+    C = torch.full((M, N), float("nan"), dtype=out_dtype, device=DEV)
+    fb.fp8bs_gemm_ws(to_dev_u8(A), to_dev_f32(sa), to_dev_u8(B), to_dev_f32(sb), sb_mode, C, ws)
+    assert fb.fp8bs_sync_status() == fb.FP8BS_OK
+    return C.float().cpu().numpy().astype(np.float64)

@@ -116,3 +116,24 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fb, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         fb.lib()
+
+
+def test_workspace_size_host_checks(L):
+    n = ctypes.c_size_t(7)
+    assert L.fp8bs_gemm_workspace_size(128, 256, 128, None) == fb.FP8BS_ERR_INVALID_ARG
+    assert L.fp8bs_gemm_workspace_size(-1, 256, 128, ctypes.byref(n)) == fb.FP8BS_ERR_INVALID_ARG
+    assert L.fp8bs_gemm_workspace_size(128, 256, 100, ctypes.byref(n)) == fb.FP8BS_ERR_UNSUPPORTED
+    assert L.fp8bs_gemm_workspace_size(0, 256, 128, ctypes.byref(n)) == fb.FP8BS_OK
+    assert n.value == 0
+
+
+def test_gemm_ws_host_checks(L):
+    # misaligned workspace, and the fp8bs_gemm checks on the same arguments
+    assert L.fp8bs_gemm_ws(128, 256, 128, FAKE, 128, FAKE, 128, FAKE, 128, FAKE,
+                           fb.FP8BS_SB_BLOCK_KN, 2, FAKE, BF16, 256, FAKE + 16, 1 << 20,
+                           None) == fb.FP8BS_ERR_MISALIGNED
+    assert L.fp8bs_gemm_ws(128, 256, 100, FAKE, 128, FAKE, 128, FAKE, 128, FAKE,
+                           fb.FP8BS_SB_BLOCK_KN, 2, FAKE, BF16, 256, NULL, 0,
+                           None) == fb.FP8BS_ERR_UNSUPPORTED
+    assert L.fp8bs_gemm_ws(0, 256, 128, NULL, 128, NULL, 128, NULL, 128, NULL,
+                           fb.FP8BS_SB_BLOCK_KN, 2, NULL, BF16, 256, NULL, 0, None) == fb.FP8BS_OK

@@ -12,29 +12,10 @@ import torch
 import fp8_fine_grained_15_b300 as fb
 import oracle
 import workloads as wl
-from gpu_helpers import (DEV, assert_gemm_close, gpu_gemm, oracle_input, to_dev_f32,
-                         to_dev_u8)
+from gpu_helpers import (DEV, MODES, assert_gemm_close, gemm_operands as _operands, gpu_gemm,
+                         oracle_input, to_dev_f32, to_dev_u8)
 
 pytestmark = pytest.mark.gpu
-
-MODES = {"KN": oracle.SB_BLOCK_KN, "NK": oracle.SB_BLOCK_NK, "PERCOL": oracle.SB_PERCOL}
-
-
-def _operands(M, N, K, mode, seed):
-    """Quantized A [M x K] (1x128) and B [N x K] with scales in `mode` layout."""
-    a = wl.random_matrix((M, K), seed=seed, dtype=torch.bfloat16)
-    Aq, sa = oracle.quant_act_1x128(oracle_input(a))
-    if mode == "PERCOL":
-        bt = wl.random_matrix((K, N), seed=seed + 1, dtype=torch.bfloat16, std=1e-3)
-        Bq, sb = oracle.quant_act_128x1(oracle_input(bt))       # [N x K], [K/128 x N]
-    else:
-        w = wl.random_matrix((K, N), seed=seed + 1, dtype=torch.bfloat16, std=0.02)
-        Wq, WqT, sw = oracle.quant_w_128x128(oracle_input(w))   # sw [K/128 x N/128]
-        Bq, sb = WqT, sw
-        if mode == "NK":
-            sb = np.ascontiguousarray(sw.T)                      # [N/128 x K/128]
-    return Aq, sa, Bq, sb
-
 
 @pytest.mark.parametrize("M,N,K,mode,out", [
     (128, 256, 128, "KN", torch.bfloat16),      # one tile, one slab
