@@ -61,13 +61,16 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_gemm_workspace_size.argtypes = [I64, I64, I64, ctypes.POINTER(ctypes.c_size_t)]
         L.fp8bs_gemm_ws.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I, I64, P, I, I64, P,
                                     ctypes.c_size_t, P]
+        L.fp8bs_gemm_static_ws.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I, I64, P, I,
+                                           I64, P]
         L.fp8bs_sync_status.argtypes = [P]
         L.fp8bs_status_string.argtypes = [I]
         L.fp8bs_status_string.restype = ctypes.c_char_p
         L.fp8bs_debug_timeout_probe.argtypes = [I64, P]
         for name in ("fp8bs_quant_act_1x128", "fp8bs_quant_act_128x1", "fp8bs_quant_w_128x128",
                      "fp8bs_gemm", "fp8bs_grouped_gemm", "fp8bs_sync_status",
-                     "fp8bs_debug_timeout_probe", "fp8bs_gemm_workspace_size", "fp8bs_gemm_ws"):
+                     "fp8bs_debug_timeout_probe", "fp8bs_gemm_workspace_size", "fp8bs_gemm_ws",
+                     "fp8bs_gemm_static_ws"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -177,6 +180,17 @@ def fp8bs_gemm_ws(A, sa, B, sb, sb_mode: int, C, workspace, stream=None):
                                _ptr(B), _row_stride(B), _ptr(sb), sb_mode, _row_stride(sb),
                                _ptr(C), _dtype(C), _row_stride(C), _ptr(workspace), ws_bytes,
                                _stream(stream)), "fp8bs_gemm_ws")
+
+
+def fp8bs_gemm_static_ws(A, sa, B, sb, sb_mode: int, C, stream=None):
+    """fp8bs_gemm_ws with the library's own 20 MiB device array as workspace
+    (allocates nothing; calls must not overlap on the GPU)."""
+    M, K = A.shape
+    N = B.shape[0]
+    _check(lib().fp8bs_gemm_static_ws(M, N, K, _ptr(A), _row_stride(A), _ptr(sa), _row_stride(sa),
+                                      _ptr(B), _row_stride(B), _ptr(sb), sb_mode, _row_stride(sb),
+                                      _ptr(C), _dtype(C), _row_stride(C), _stream(stream)),
+           "fp8bs_gemm_static_ws")
 
 
 def fp8bs_grouped_gemm(offsets, A, sa, B, sb, sb_mode: int, C, stream=None):

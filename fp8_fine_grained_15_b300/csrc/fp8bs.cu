@@ -15,10 +15,37 @@
 #include "gemm_pair_kernel.cuh"
 #include "quant_kernels.cuh"
 
+// Scratch of fp8bs_gemm_static_ws, for callers that cannot allocate device
+// memory: the FP32 partials of the split last wave live here instead of in a
+// caller workspace.  Every GPU that loads the library holds these 20 MiB until
+// the process exits; every call shares them (see include/fp8bs.h).
+static __device__ __align__(256) unsigned char fp8bs_static_ws[20u << 20];
+
 namespace fp8bs {
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr size_t kStaticWsBytes = sizeof(fp8bs_static_ws);
+
+// Device address of fp8bs_static_ws on the current device, looked up once per
+// device (with that device current).  In host code the array's name is only a
+// host-side stand-in, never a device address.
+void* g_static_ws_addr[kMaxDevices] = {};
+
+fp8bs_status static_workspace(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8BS_ERR_CUDA;
+  static std::mutex m;
+  std::lock_guard<std::mutex> lock(m);
+  if (g_static_ws_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, fp8bs_static_ws) != cudaSuccess || ptr == nullptr)
+      return FP8BS_ERR_CUDA;
+    g_static_ws_addr[dev] = ptr;
+  }
+  *out = g_static_ws_addr[dev];
+  return FP8BS_OK;
+}
 
 struct DeviceInfo {
   bool init = false;
@@ -495,6 +522,20 @@ fp8bs_status fp8bs_gemm_ws(int64_t M, int64_t N, int64_t K, const uint8_t* A, in
   if (workspace != nullptr && !aligned(workspace, 256)) return FP8BS_ERR_MISALIGNED;
   return gemm_dense(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc,
                     static_cast<float*>(workspace), workspace ? workspace_bytes : 0, stream);
+}
+
+fp8bs_status fp8bs_gemm_static_ws(int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                                  int64_t lda, const float* sa, int64_t ldsa, const uint8_t* B,
+                                  int64_t ldb, const float* sb, fp8bs_bscale sb_mode, int64_t ldsb,
+                                  void* C, fp8bs_dtype ct, int64_t ldc, void* stream) {
+  size_t need = 0;
+  fp8bs_status st = fp8bs_gemm_workspace_size(M, N, K, &need);
+  if (st != FP8BS_OK) return st;
+  if (need > kStaticWsBytes) return FP8BS_ERR_UNSUPPORTED;   // more scratch than the array holds
+  void* ws = nullptr;
+  if ((st = static_workspace(&ws)) != FP8BS_OK) return st;
+  return gemm_dense(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc,
+                    static_cast<float*>(ws), kStaticWsBytes, stream);
 }
 
 fp8bs_status fp8bs_grouped_gemm(int32_t E, const int32_t* offsets, int64_t M_cap, int64_t N,

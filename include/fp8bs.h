@@ -160,6 +160,30 @@ fp8bs_status fp8bs_gemm_ws(int64_t M, int64_t N, int64_t K,
                            int64_t ldsb, void* C, fp8bs_dtype ct, int64_t ldc, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* fp8bs_gemm_ws for callers that cannot allocate device memory: some cannot
+ * call cudaMalloc at all where they run (e.g. code that may not synchronize
+ * the device or bypass the memory pool of the framework around it), and some
+ * hold only their operand buffers and have no workspace to lend.  This entry
+ * point allocates nothing: the K split's FP32 partials go to a 20 MiB array in
+ * the library's own device memory, which every GPU that loads the library
+ * holds until the process exits.  The paper has no counterpart of this call.
+ *   Arguments, requirements and results are those of fp8bs_gemm_ws with a
+ *   20 MiB workspace (the split is chosen the same way).
+ *   A shape whose fp8bs_gemm_workspace_size exceeds 20 MiB is rejected with
+ *   FP8BS_ERR_UNSUPPORTED before any launch (on a 148-SM B300 no shape needs
+ *   more than 74 partial tiles, 18.5 MiB).
+ *   The first call on a device looks up the array's device address (the
+ *   device must be current); make that first call before any stream capture.
+ *   Every call uses the same array and it keeps the last call's partials; a
+ *   call writes every partial it reads, so nothing needs clearing.  Calls that
+ *   overlap on the GPU (other streams, other host threads) race on the array:
+ *   order them on one stream. */
+fp8bs_status fp8bs_gemm_static_ws(int64_t M, int64_t N, int64_t K,
+                                  const uint8_t* A, int64_t lda, const float* sa, int64_t ldsa,
+                                  const uint8_t* B, int64_t ldb, const float* sb,
+                                  fp8bs_bscale sb_mode, int64_t ldsb, void* C, fp8bs_dtype ct,
+                                  int64_t ldc, void* stream);
+
 /* Grouped block-scaled FP8 GEMM for MoE experts: expert e owns rows
  * offsets[e] .. offsets[e+1]-1 of A and C and multiplies them by B[e]:
  *   C[i][:] = A[i][:] * B[e]^T with the scales sa (rows) and sb + e*sb_estride.
