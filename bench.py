@@ -2,9 +2,10 @@
 
 One step = one training pass of a linear layer (tokens 4096, K_in 7168,
 N_out 18432) through every row of the path:
-    quant 1x128 (X) -> quant 128x128 (W, with transposed copy) -> Fprop GEMM
-    quant 1x128 (dY) -> Dgrad GEMM
-    quant 128x1 (X), quant 128x1 (dY) -> Wgrad GEMM (FP32 out)
+    quant 1x128 + 128x1 of X (one pass) -> quant 128x128 (W, with transposed
+    copy) -> Fprop GEMM -> quant 1x128 + 128x1 of dY (one pass) -> Dgrad GEMM
+    -> Wgrad GEMM (FP32 out)
+The GEMMs split the K range of their last, partial wave (fp8bs_gemm_ws).
 `value` = the three GEMMs' FLOPs (3 x 2*M*N*K) / device time of the whole step,
 in TFLOPS, with inputs resident in HBM.  Per-kernel CUDA-event timings give the
 roofline of the dominant kernel and of every other launch.  `e2e` repeats the
@@ -46,6 +47,11 @@ WORKLOAD = ("linear-layer training step: quant 1x128/128x1/128x128 + Fprop, Dgra
 def quant_bytes(elems: int, in_bytes: int, transposed_copy: bool = False, block=False) -> float:
     scale = 4.0 / (128 * 128) if block else 4.0 / 128
     return elems * (in_bytes + 1 + (1 if transposed_copy else 0) + scale)
+
+
+def dual_bytes(elems: int, in_bytes: int) -> float:
+    """One read of the input, both code copies, both scale arrays."""
+    return elems * (in_bytes + 2 + 2 * 4.0 / 128)
 
 
 # DRAM traffic per launch measured by ncu (dram__bytes_read.sum + write.sum), with
@@ -129,8 +135,8 @@ class ClockSampler:
 class LayerStep:
     """Device buffers and the launch sequence of one layer training step."""
 
-    KERNELS = ["quant_1x128_X", "quant_128x128_W", "gemm_fprop", "quant_1x128_dY",
-               "gemm_dgrad", "quant_128x1_X", "quant_128x1_dY", "gemm_wgrad"]
+    KERNELS = ["quant_dual_X", "quant_128x128_W", "gemm_fprop", "quant_dual_dY",
+               "gemm_dgrad", "gemm_wgrad"]
 
     def __init__(self, x, w, dy, dev):
         import fp8_fine_grained_15_b300 as fb
@@ -156,31 +162,28 @@ class LayerStep:
     def launches(self):
         fb = self.fb
         return [
-            lambda s: fb.fp8bs_quant_act_1x128(self.x, self.Xq, self.Sx, s),
+            lambda s: fb.fp8bs_quant_act_dual(self.x, self.Xq, self.Sx, self.XqT, self.SxT, s),
             lambda s: fb.fp8bs_quant_w_128x128(self.w, self.Wq, self.WqT, self.Sw, s),
             lambda s: fb.fp8bs_gemm_ws(self.Xq, self.Sx, self.WqT, self.Sw, fb.FP8BS_SB_BLOCK_KN,
                                        self.Y, self.ws, s),
-            lambda s: fb.fp8bs_quant_act_1x128(self.dy, self.dYq, self.Sdy, s),
+            lambda s: fb.fp8bs_quant_act_dual(self.dy, self.dYq, self.Sdy, self.dYqT, self.SdyT, s),
             lambda s: fb.fp8bs_gemm_ws(self.dYq, self.Sdy, self.Wq, self.Sw, fb.FP8BS_SB_BLOCK_NK,
                                        self.dX, self.ws, s),
-            lambda s: fb.fp8bs_quant_act_128x1(self.x, self.XqT, self.SxT, s),
-            lambda s: fb.fp8bs_quant_act_128x1(self.dy, self.dYqT, self.SdyT, s),
             lambda s: fb.fp8bs_gemm_ws(self.XqT, self.SxT, self.dYqT, self.SdyT,
                                        fb.FP8BS_SB_PERCOL, self.dW, self.ws, s),
         ]
 
     def kernel_launches(self):
-        """Library kernels one step launches: 5 quantizers, 3 GEMMs, plus the
+        """Library kernels one step launches: 3 quantizers, 3 GEMMs, plus the
         partial-sum kernel of each GEMM whose last wave is split."""
-        return 8 + sum(1 for n in self.ws_need if n > 0)
+        return 6 + sum(1 for n in self.ws_need if n > 0)
 
     def work(self):
         """(kind, algorithmic amount) per launch: bytes for quantizers, FLOPs for GEMMs."""
         T, K, N = self.T, self.K, self.N
         g = 2.0 * T * K * N
-        return [("hbm", quant_bytes(T * K, 2)), ("hbm", quant_bytes(K * N, 2, True, True)),
-                ("tensor", g), ("hbm", quant_bytes(T * N, 2)), ("tensor", g),
-                ("hbm", quant_bytes(T * K, 2)), ("hbm", quant_bytes(T * N, 2)), ("tensor", g)]
+        return [("hbm", dual_bytes(T * K, 2)), ("hbm", quant_bytes(K * N, 2, True, True)),
+                ("tensor", g), ("hbm", dual_bytes(T * N, 2)), ("tensor", g), ("tensor", g)]
 
 
 def _barrier(dist_on):
@@ -388,12 +391,17 @@ def run_extras(dev, stream, peaks):
         nbytes = quant_bytes(M * wl.HIDDEN, 2)
         m1, _ = timeit(lambda: fb.fp8bs_quant_act_1x128(x, q, s, stream), flush=flush)
         m2, _ = timeit(lambda: fb.fp8bs_quant_act_128x1(x, qT, sT, stream), flush=flush)
+        m3, _ = timeit(lambda: fb.fp8bs_quant_act_dual(x, q, s, qT, sT, stream), flush=flush)
+        dbytes = dual_bytes(M * wl.HIDDEN, 2)
         sweep[f"M{M}"] = {
             "bytes": int(nbytes),
             "1x128_us": round(m1 * 1e3, 2), "1x128_GB/s": round(nbytes / (m1 * 1e-3) / 1e9, 1),
             "1x128_frac_hbm": round(nbytes / (m1 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "128x1_us": round(m2 * 1e3, 2), "128x1_GB/s": round(nbytes / (m2 * 1e-3) / 1e9, 1),
-            "128x1_frac_hbm": round(nbytes / (m2 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+            "128x1_frac_hbm": round(nbytes / (m2 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "dual_bytes": int(dbytes), "dual_us": round(m3 * 1e3, 2),
+            "dual_GB/s": round(dbytes / (m3 * 1e-3) / 1e9, 1),
+            "dual_frac_hbm": round(dbytes / (m3 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
         del x, q, s, qT, sT
     wgt = torch.randn((wl.HIDDEN, wl.FFN), device=dev, generator=gen).to(torch.bfloat16)
     wq = torch.empty((wl.HIDDEN, wl.FFN), dtype=torch.uint8, device=dev)
@@ -470,7 +478,8 @@ def run_reference(args, rank, world, dist_on):
     }
 
 
-CASES = ("fprop", "dgrad", "wgrad", "grouped", "quant_1x128", "quant_128x1", "quant_128x128")
+CASES = ("fprop", "dgrad", "wgrad", "grouped", "quant_1x128", "quant_128x1", "quant_dual",
+         "quant_128x128")
 
 
 def run_case(args):
@@ -536,13 +545,17 @@ def run_case(args):
             amount = quant_bytes(K * N, 2, True, True)
         else:
             x = torch.randn((M, K), device=dev, generator=gen).to(torch.bfloat16)
+            amount = quant_bytes(M * K, 2)
             if c == "quant_1x128":
                 q, s = u8(M, K), f32(K // 128, M)
                 fn = lambda: fb.fp8bs_quant_act_1x128(x, q, s, stream)  # noqa: E731
-            else:
+            elif c == "quant_128x1":
                 q, s = u8(K, M), f32(M // 128, K)
                 fn = lambda: fb.fp8bs_quant_act_128x1(x, q, s, stream)  # noqa: E731
-            amount = quant_bytes(M * K, 2)
+            else:
+                q, s, qT, sT = u8(M, K), f32(K // 128, M), u8(K, M), f32(M // 128, K)
+                fn = lambda: fb.fp8bs_quant_act_dual(x, q, s, qT, sT, stream)  # noqa: E731
+                amount = dual_bytes(M * K, 2)
         kind = "hbm"
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > L2
     for _ in range(args.warmup):

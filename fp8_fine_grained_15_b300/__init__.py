@@ -55,6 +55,9 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_quant_act_1x128.argtypes = [P, I, I64, I64, I64, P, I64, P, I64, P]
         L.fp8bs_quant_act_128x1.argtypes = [P, I, I64, I64, I64, P, I64, P, I64, P]
         L.fp8bs_quant_w_128x128.argtypes = [P, I, I64, I64, I64, P, I64, P, I64, P, I64, P]
+        L.fp8bs_gemm_accumulate.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I, I64, P,
+                                            I64, P, ctypes.c_size_t, P]
+        L.fp8bs_quant_act_dual.argtypes = [P, I, I64, I64, I64, P, I64, P, I64, P, I64, P, I64, P]
         L.fp8bs_gemm.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I, I64, P, I, I64, P]
         L.fp8bs_grouped_gemm.argtypes = [I32, P, I64, I64, I64, P, I64, P, I64, P, I64, P, I,
                                          I64, I64, P, I, I64, P]
@@ -70,7 +73,7 @@ def lib() -> ctypes.CDLL:
         for name in ("fp8bs_quant_act_1x128", "fp8bs_quant_act_128x1", "fp8bs_quant_w_128x128",
                      "fp8bs_gemm", "fp8bs_grouped_gemm", "fp8bs_sync_status",
                      "fp8bs_debug_timeout_probe", "fp8bs_gemm_workspace_size", "fp8bs_gemm_ws",
-                     "fp8bs_gemm_static_ws"):
+                     "fp8bs_gemm_static_ws", "fp8bs_quant_act_dual", "fp8bs_gemm_accumulate"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -144,6 +147,16 @@ def fp8bs_quant_act_128x1(x, qT, s, stream=None):
                                        _stream(stream)), "fp8bs_quant_act_128x1")
 
 
+def fp8bs_quant_act_dual(x, q, s, qT, sT, stream=None):
+    """x [T x C] -> q [T x C] + s [C/128 x >=T] (1x128) and qT [C x T] +
+    sT [T/128 x >=C] (128x1), from one read of x."""
+    T, C = x.shape
+    _check(lib().fp8bs_quant_act_dual(_ptr(x), _dtype(x), T, C, _row_stride(x), _ptr(q),
+                                      _row_stride(q), _ptr(s), _row_stride(s), _ptr(qT),
+                                      _row_stride(qT), _ptr(sT), _row_stride(sT),
+                                      _stream(stream)), "fp8bs_quant_act_dual")
+
+
 def fp8bs_quant_w_128x128(w, q, qT, s, stream=None):
     """w [R x C] -> q [R x C] (or None), qT [C x R] (or None), s [R/128 x lds>=C/128]."""
     R, C = w.shape
@@ -180,6 +193,20 @@ def fp8bs_gemm_ws(A, sa, B, sb, sb_mode: int, C, workspace, stream=None):
                                _ptr(B), _row_stride(B), _ptr(sb), sb_mode, _row_stride(sb),
                                _ptr(C), _dtype(C), _row_stride(C), _ptr(workspace), ws_bytes,
                                _stream(stream)), "fp8bs_gemm_ws")
+
+
+def fp8bs_gemm_accumulate(A, sa, B, sb, sb_mode: int, C, workspace=None, stream=None):
+    """C (fp32) += block-scaled A * B^T; workspace as in fp8bs_gemm_ws."""
+    M, K = A.shape
+    N = B.shape[0]
+    if C.dtype != __import__("torch").float32:
+        raise TypeError("fp8bs_gemm_accumulate needs a float32 C")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fp8bs_gemm_accumulate(M, N, K, _ptr(A), _row_stride(A), _ptr(sa),
+                                       _row_stride(sa), _ptr(B), _row_stride(B), _ptr(sb),
+                                       sb_mode, _row_stride(sb), _ptr(C), _row_stride(C),
+                                       _ptr(workspace), ws_bytes, _stream(stream)),
+           "fp8bs_gemm_accumulate")
 
 
 def fp8bs_gemm_static_ws(A, sa, B, sb, sb_mode: int, C, stream=None):

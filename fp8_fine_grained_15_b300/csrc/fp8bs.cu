@@ -253,7 +253,7 @@ SplitPlan plan_split(int tiles, int KB, int clusters, size_t ws_avail) {
 
 fp8bs_status launch_gemm_pair(GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& tc, const CUtensorMap& tws, const float* ws,
-                              int tail, int clusters, int sb_kind, fp8bs_dtype ct,
+                              int tail, int clusters, int sb_kind, fp8bs_dtype ct, bool acc,
                               cudaStream_t stream) {
   auto run = [&](auto kernel) -> fp8bs_status {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -266,11 +266,16 @@ fp8bs_status launch_gemm_pair(GemmParams& p, const CUtensorMap& ta, const CUtens
     const unsigned blocks = static_cast<unsigned>(tail) * (kPairTileM * 64 / 256);
     if (ct == FP8BS_BF16)
       split_fixup_kernel<true><<<blocks, 256, 0, stream>>>(ws, p, tail);
+    else if (acc)
+      split_fixup_kernel<false, true><<<blocks, 256, 0, stream>>>(ws, p, tail);
     else
       split_fixup_kernel<false><<<blocks, 256, 0, stream>>>(ws, p, tail);
     return launch_status();
   };
   const bool bf16 = ct == FP8BS_BF16;
+  if (acc)   // FP32 output only
+    return sb_kind == kSbBlock ? run(fp8bs_gemm_pair_kernel<kSbBlock, false, true>)
+                               : run(fp8bs_gemm_pair_kernel<kSbPerCol, false, true>);
   if (sb_kind == kSbBlock)
     return bf16 ? run(fp8bs_gemm_pair_kernel<kSbBlock, true>)
                 : run(fp8bs_gemm_pair_kernel<kSbBlock, false>);
@@ -280,7 +285,8 @@ fp8bs_status launch_gemm_pair(GemmParams& p, const CUtensorMap& ta, const CUtens
 
 template <bool kGrouped>
 fp8bs_status launch_gemm(GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                         int sb_kind, fp8bs_dtype ct, cudaStream_t stream) {
+                         const CUtensorMap& tc, int sb_kind, fp8bs_dtype ct,
+                         cudaStream_t stream) {
   DeviceInfo di;
   fp8bs_status st = device_info(&di);
   if (st != FP8BS_OK) return st;
@@ -290,7 +296,7 @@ fp8bs_status launch_gemm(GemmParams& p, const CUtensorMap& ta, const CUtensorMap
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kGemmSmemBytes)) != cudaSuccess)
       return FP8BS_ERR_CUDA;
-    kernel<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p, ta, tb);
+    kernel<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p, ta, tb, tc);
     return launch_status();
   };
   const bool bf16 = ct == FP8BS_BF16;
@@ -367,10 +373,11 @@ void launch_quant_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_
 fp8bs_status gemm_dense(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
                         const float* sa, int64_t ldsa, const uint8_t* B, int64_t ldb,
                         const float* sb, fp8bs_bscale sb_mode, int64_t ldsb, void* C,
-                        fp8bs_dtype ct, int64_t ldc, float* ws, size_t ws_bytes, void* stream) {
+                        fp8bs_dtype ct, int64_t ldc, float* ws, size_t ws_bytes, void* stream,
+                        bool acc = false) {
   fp8bs_status st = check_gemm(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc);
   if (st != FP8BS_OK || M == 0 || N == 0) return st;
-  if (K == 0) return zero_fill(C, ct, M, N, ldc, as_stream(stream));
+  if (K == 0) return acc ? FP8BS_OK : zero_fill(C, ct, M, N, ldc, as_stream(stream));
   CUtensorMap ta, tb, tc;
   if ((st = make_map_2d(&ta, A, K, M, lda, kBM)) != FP8BS_OK) return st;
   if ((st = make_map_2d(&tb, B, K, N, ldb, kBN / 2)) != FP8BS_OK) return st;
@@ -403,7 +410,8 @@ fp8bs_status gemm_dense(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
                          static_cast<uint64_t>(sp.tail) * sp.splits * kPairTileM, kBN)) != FP8BS_OK)
     return st;
   return launch_gemm_pair(p, ta, tb, tc, tws, ws, sp.tail, clusters,
-                          sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct, as_stream(stream));
+                          sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct, acc,
+                          as_stream(stream));
 }
 
 }  // namespace
@@ -457,6 +465,37 @@ fp8bs_status fp8bs_quant_act_128x1(const void* x, fp8bs_dtype xt, int64_t T, int
     prefer_max_shared(quant_128x1_kernel<float>);
     quant_128x1_kernel<float><<<grid, 256, 0, as_stream(stream)>>>(static_cast<const float*>(x),
                                                                    C, ldx, qT, ldq, s, lds);
+  }
+  return launch_status();
+}
+
+fp8bs_status fp8bs_quant_act_dual(const void* x, fp8bs_dtype xt, int64_t T, int64_t C,
+                                  int64_t ldx, uint8_t* q, int64_t ldq, float* s, int64_t lds,
+                                  uint8_t* qT, int64_t ldqT, float* sT, int64_t ldsT,
+                                  void* stream) {
+  if (T < 0 || C < 0 || !valid_dtype(xt)) return FP8BS_ERR_INVALID_ARG;
+  if (T % 128 != 0 || C % 128 != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (T == 0 || C == 0) return FP8BS_OK;
+  if (T / 128 > 65535 || C / 128 > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+  if (x == nullptr || q == nullptr || s == nullptr || qT == nullptr || sT == nullptr)
+    return FP8BS_ERR_INVALID_ARG;
+  if (ldx < C || ldq < C || lds < T || ldqT < T || ldsT < C) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (ldx * static_cast<int64_t>(dtype_size(xt))) % 16 || !aligned(q, 16) ||
+      ldq % 16 || !aligned(qT, 16) || ldqT % 16 || !aligned(s, 4) || !aligned(sT, 4))
+    return FP8BS_ERR_MISALIGNED;
+  dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(T / 128));
+  const size_t smem = 128 * 128 * dtype_size(xt);
+  if (xt == FP8BS_BF16) {
+    prefer_max_shared(quant_dual_kernel<__nv_bfloat16>);
+    quant_dual_kernel<__nv_bfloat16><<<grid, 256, smem, as_stream(stream)>>>(
+        static_cast<const __nv_bfloat16*>(x), ldx, q, ldq, s, lds, qT, ldqT, sT, ldsT);
+  } else {
+    if (cudaFuncSetAttribute(quant_dual_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
+    prefer_max_shared(quant_dual_kernel<float>);
+    quant_dual_kernel<float><<<grid, 256, smem, as_stream(stream)>>>(
+        static_cast<const float*>(x), ldx, q, ldq, s, lds, qT, ldqT, sT, ldsT);
   }
   return launch_status();
 }
@@ -524,6 +563,17 @@ fp8bs_status fp8bs_gemm_ws(int64_t M, int64_t N, int64_t K, const uint8_t* A, in
                     static_cast<float*>(workspace), workspace ? workspace_bytes : 0, stream);
 }
 
+fp8bs_status fp8bs_gemm_accumulate(int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                                   int64_t lda, const float* sa, int64_t ldsa, const uint8_t* B,
+                                   int64_t ldb, const float* sb, fp8bs_bscale sb_mode,
+                                   int64_t ldsb, float* C, int64_t ldc, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (workspace != nullptr && !aligned(workspace, 256)) return FP8BS_ERR_MISALIGNED;
+  return gemm_dense(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, FP8BS_F32, ldc,
+                    static_cast<float*>(workspace), workspace ? workspace_bytes : 0, stream,
+                    /*acc=*/true);
+}
+
 fp8bs_status fp8bs_gemm_static_ws(int64_t M, int64_t N, int64_t K, const uint8_t* A,
                                   int64_t lda, const float* sa, int64_t ldsa, const uint8_t* B,
                                   int64_t ldb, const float* sb, fp8bs_bscale sb_mode, int64_t ldsb,
@@ -552,9 +602,10 @@ fp8bs_status fp8bs_grouped_gemm(int32_t E, const int32_t* offsets, int64_t M_cap
   if (st != FP8BS_OK || M_cap == 0 || N == 0) return st;
   if (sb_mode == FP8BS_SB_PERCOL && sb_estride % 4 != 0) return FP8BS_ERR_MISALIGNED;
   if (K == 0) return FP8BS_ERR_UNSUPPORTED;  // expert rows are only known on the device
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if ((st = make_map_2d(&ta, A, K, M_cap, lda, kBM)) != FP8BS_OK) return st;
   if ((st = make_map_3d(&tb, B, K, N, E, ldb, kBN)) != FP8BS_OK) return st;
+  if ((st = make_map_out(&tc, C, ct, N, M_cap, ldc)) != FP8BS_OK) return st;
   GemmParams p{};
   p.M = static_cast<int32_t>(M_cap);
   p.N = static_cast<int32_t>(N);
@@ -570,7 +621,7 @@ fp8bs_status fp8bs_grouped_gemm(int32_t E, const int32_t* offsets, int64_t M_cap
   p.C = C;
   p.ldc = ldc;
   p.offsets = offsets;
-  return launch_gemm<true>(p, ta, tb, sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct,
+  return launch_gemm<true>(p, ta, tb, tc, sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct,
                            as_stream(stream));
 }
 

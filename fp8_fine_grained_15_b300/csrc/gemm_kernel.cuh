@@ -51,6 +51,7 @@ static_assert(128 * kProducerRegs + 256 * kEpilogueRegs <= 168 * kGemmThreads,
 constexpr int kMaxExperts = 1024;
 
 enum SbKind : int { kSbBlock = 0, kSbPerCol = 1 };
+constexpr int kEpiStageBytes = 32 * 64;   // one warp's output chunk: 32 rows x 64 B
 
 struct GemmParams {
   int32_t M;            // rows of A / C (M_cap for the grouped call)
@@ -77,6 +78,7 @@ struct GemmParams {
 };
 
 struct GemmSmem {
+  alignas(1024) unsigned char epi_stage[kEpiWarps][kEpiStageBytes];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t tfull[2];
@@ -157,11 +159,55 @@ __device__ __forceinline__ void promote32_percol(float2* acc, const uint32_t (&r
   }
 }
 
+// Store this warp's 32 rows x 128 accumulator columns (row `lane` per
+// thread) through a 2 KB shared buffer and 64-byte-wide TMA boxes at (col, row)
+// of `tmap`: FP32 (16 columns per box) or BF16 rounded to nearest even (32).
+// kAdd: the FP32 boxes are added into the existing values instead.
+template <bool kBf16, bool kAdd = false>
+__device__ __forceinline__ void store_rows_tma(const float2* acc, uint32_t stg, int lane,
+                                               const CUtensorMap* tmap, int col, int row) {
+  constexpr int kChunkCols = kBf16 ? 32 : 16;   // 64 bytes of output per row
+#pragma unroll
+  for (int c = 0; c < 128 / kChunkCols; ++c) {
+    // the previous bulk store of this buffer must have read it
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // 16-byte unit j of this row's 64 bytes
+      // row `lane` at 64 * lane; 16-byte unit j at position j ^ ((lane >> 1) & 3)
+      const uint32_t dst = stg + static_cast<uint32_t>(lane) * 64u +
+                           ((static_cast<uint32_t>(j) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u)) << 4);
+      if constexpr (kBf16) {
+        const int k = c * 16 + 4 * j;   // float2 index of column c*32 + 8j
+        st_shared_v4(dst, make_uint4(pack_bf16x2(acc[k].x, acc[k].y),
+                                     pack_bf16x2(acc[k + 1].x, acc[k + 1].y),
+                                     pack_bf16x2(acc[k + 2].x, acc[k + 2].y),
+                                     pack_bf16x2(acc[k + 3].x, acc[k + 3].y)));
+      } else {
+        // two 8-byte stores straight from the accumulator register pairs
+        const int k = c * 8 + 2 * j;    // float2 index of column c*16 + 4j
+        st_shared_v2f(dst, acc[k]);
+        st_shared_v2f(dst + 8, acc[k + 1]);
+      }
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (kAdd)
+        tma_reduce_add_2d(tmap, col + c * kChunkCols, row, stg);
+      else
+        tma_store_2d(tmap, col + c * kChunkCols, row, stg);
+      bulk_commit_group();
+    }
+  }
+}
+
 template <bool kGrouped, int kSb, bool kOutBf16>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fp8bs_gemm_kernel(const __grid_constant__ GemmParams p,
                       const __grid_constant__ CUtensorMap tmap_a,
-                      const __grid_constant__ CUtensorMap tmap_b) {
+                      const __grid_constant__ CUtensorMap tmap_b,
+                      const __grid_constant__ CUtensorMap tmap_c) {
   extern __shared__ __align__(1024) unsigned char gemm_smem_raw[];
   // 1024-byte aligned operand ring (the 128-byte swizzle atoms need it)
   const uint32_t raw_addr = smem_u32(gemm_smem_raw);
@@ -189,6 +235,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_mbarrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
+    tma_prefetch_desc(&tmap_c);
   }
   if constexpr (kGrouped) {
     // Stage and validate the expert offsets (every CTA, so none depends on another).
@@ -403,33 +450,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         sa_cur = sa_nxt;
         sb_cur = sb_nxt;
       }
-      // ---- epilogue: this thread's row, 128 columns
-      if (row_ok && cols_ok) {
-        if constexpr (kOutBf16) {
-          __nv_bfloat16* crow = reinterpret_cast<__nv_bfloat16*>(p.C) +
-                                static_cast<int64_t>(row) * p.ldc + col0;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {  // 8 columns per 16-byte store
-            if (kSb == kSbPerCol && col0 + c * 8 >= p.N) break;
-            uint4 o;
-            o.x = pack_bf16x2(acc[4 * c].x, acc[4 * c].y);
-            o.y = pack_bf16x2(acc[4 * c + 1].x, acc[4 * c + 1].y);
-            o.z = pack_bf16x2(acc[4 * c + 2].x, acc[4 * c + 2].y);
-            o.w = pack_bf16x2(acc[4 * c + 3].x, acc[4 * c + 3].y);
-            *reinterpret_cast<uint4*>(crow + c * 8) = o;
-          }
-        } else {
-          float* crow = reinterpret_cast<float*>(p.C) + static_cast<int64_t>(row) * p.ldc + col0;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {  // 4 columns per 16-byte store
-            if (kSb == kSbPerCol && col0 + c * 4 >= p.N) break;
-            *reinterpret_cast<float4*>(crow + c * 4) =
-                make_float4(acc[2 * c].x, acc[2 * c].y, acc[2 * c + 1].x, acc[2 * c + 1].y);
-          }
-        }
-      }
+      // ---- epilogue: this warp's 32 rows x 128 columns, through TMA stores
+      // (rows of a tile never straddle two experts: expert ranges are whole tiles)
+      store_rows_tma<kOutBf16>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_c, col0,
+                               tc.m0 + g * 32);
     }
-  epilogue_done:;
+  epilogue_done:
+    if (lane == 0) bulk_wait_all();   // this warp's output stores are complete
     }
   }
 

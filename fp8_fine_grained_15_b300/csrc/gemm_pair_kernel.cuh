@@ -47,8 +47,6 @@ constexpr uint32_t kPairEpilogueRegs = 232;
 static_assert(128 * kPairProducerRegs + 256 * kPairEpilogueRegs <= 168 * kGemmThreads,
               "register split exceeds the launch budget");
 
-constexpr int kEpiStageBytes = 32 * 64;       // one warp's output chunk: 32 rows x 64 B
-
 struct PairSmem {
   alignas(1024) unsigned char epi_stage[kEpiWarps][kEpiStageBytes];
   uint64_t full[kPairStages];   // even CTA: both CTAs' loads of a slab have landed
@@ -90,48 +88,10 @@ __device__ __forceinline__ PairUnit pair_unit(int u, const GemmParams& p) {
   return w;
 }
 
-// Store this warp's 32 rows x 128 accumulator columns (row `lane` per
-// thread) through a 2 KB shared buffer and 64-byte-wide TMA boxes at (col, row)
-// of `tmap`: FP32 (16 columns per box) or BF16 rounded to nearest even (32).
-template <bool kBf16>
-__device__ __forceinline__ void store_rows_tma(const float2* acc, uint32_t stg, int lane,
-                                               const CUtensorMap* tmap, int col, int row) {
-  constexpr int kChunkCols = kBf16 ? 32 : 16;   // 64 bytes of output per row
-#pragma unroll
-  for (int c = 0; c < 128 / kChunkCols; ++c) {
-    // the previous bulk store of this buffer must have read it
-    if (lane == 0) bulk_wait_read_all();
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {   // 16-byte unit j of this row's 64 bytes
-      // row `lane` at 64 * lane; 16-byte unit j at position j ^ ((lane >> 1) & 3)
-      const uint32_t dst = stg + static_cast<uint32_t>(lane) * 64u +
-                           ((static_cast<uint32_t>(j) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u)) << 4);
-      if constexpr (kBf16) {
-        const int k = c * 16 + 4 * j;   // float2 index of column c*32 + 8j
-        st_shared_v4(dst, make_uint4(pack_bf16x2(acc[k].x, acc[k].y),
-                                     pack_bf16x2(acc[k + 1].x, acc[k + 1].y),
-                                     pack_bf16x2(acc[k + 2].x, acc[k + 2].y),
-                                     pack_bf16x2(acc[k + 3].x, acc[k + 3].y)));
-      } else {
-        // two 8-byte stores straight from the accumulator register pairs
-        const int k = c * 8 + 2 * j;    // float2 index of column c*16 + 4j
-        st_shared_v2f(dst, acc[k]);
-        st_shared_v2f(dst + 8, acc[k + 1]);
-      }
-    }
-    fence_proxy_async_shared();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(tmap, col + c * kChunkCols, row, stg);
-      bulk_commit_group();
-    }
-  }
-}
-
 // Sum of the K-range partials of the tail tiles, in split order, converted to
-// the output type.  One thread per 4 columns of one row of one tail tile.
-template <bool kOutBf16>
+// the output type (kAcc: added to the FP32 values already in C).  One thread
+// per 4 columns of one row of one tail tile.
+template <bool kOutBf16, bool kAcc = false>
 __global__ void __launch_bounds__(256) split_fixup_kernel(const float* __restrict__ ws,
                                                           GemmParams p, int tail_tiles) {
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -156,13 +116,19 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(const float* __restric
     __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(p.C) + static_cast<int64_t>(row) * p.ldc + col;
     *reinterpret_cast<uint2*>(c) = make_uint2(pack_bf16x2(sum.x, sum.y), pack_bf16x2(sum.z, sum.w));
   } else {
-    float* c = reinterpret_cast<float*>(p.C) + static_cast<int64_t>(row) * p.ldc + col;
-    *reinterpret_cast<float4*>(c) = sum;
+    float4* c = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.C) +
+                                          static_cast<int64_t>(row) * p.ldc + col);
+    if constexpr (kAcc) {
+      const float4 old = *c;
+      sum = make_float4(old.x + sum.x, old.y + sum.y, old.z + sum.z, old.w + sum.w);
+    }
+    *c = sum;
   }
 }
 
-// p.num_m_tiles counts 256-row pair tiles here.
-template <int kSb, bool kOutBf16>
+// p.num_m_tiles counts 256-row pair tiles here.  kAcc (FP32 output only):
+// C += A * B^T, the tiles added into C by TMA reduce-add.
+template <int kSb, bool kOutBf16, bool kAcc = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     fp8bs_gemm_pair_kernel(const __grid_constant__ GemmParams p,
                            const __grid_constant__ CUtensorMap tmap_a,
@@ -387,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // (addresses are recomputed, not held: the promotion warps have no
       // registers to spare while the accumulators are live)
       if (w.slot < 0) {
-        store_rows_tma<kOutBf16>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_c, col0,
+        store_rows_tma<kOutBf16, kAcc>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_c, col0,
                                  (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM + g * 32);
       } else {
         store_rows_tma<false>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_ws, h * 128,

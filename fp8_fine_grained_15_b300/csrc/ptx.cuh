@@ -165,6 +165,16 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t c0, int32
       "r"(c0), "r"(c1), "r"(src_smem)
       : "memory");
 }
+// Same box, added element-wise into global memory (the add happens in L2;
+// the element type, here FP32, comes from the tensor map).
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, int32_t c0, int32_t c1,
+                                                  uint32_t src_smem) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(src_smem)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

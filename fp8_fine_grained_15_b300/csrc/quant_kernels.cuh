@@ -167,8 +167,8 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const TIn* __restrict_
 // thread then owns one 32-bit channel group (two bf16 channels or one fp32
 // channel) and 32 consecutive tokens: 32 conflict-free word reads, a
 // per-channel partial amax combined across the four token parts through shared
-// memory, then 32 codes per channel written as two 16-byte runs of the
-// transposed output.
+// memory, then 32 codes per channel (words re-read from shared memory) written
+// as two 16-byte runs of the transposed output.
 template <typename TIn>
 __global__ void __launch_bounds__(256, 4) quant_128x1_kernel(const TIn* __restrict__ x, int64_t C,
                                                              int64_t ldx, uint8_t* __restrict__ qT,
@@ -211,18 +211,17 @@ __global__ void __launch_bounds__(256, 4) quant_128x1_kernel(const TIn* __restri
 
   const int g = tid % kGroups;
   const int part = tid / kGroups;
-  uint32_t w[kTok];
   float amax[kCh];
 #pragma unroll
   for (int k = 0; k < kCh; ++k) amax[k] = 0.0f;
-#pragma unroll
+#pragma unroll 8
   for (int t = 0; t < kTok; ++t) {
-    w[t] = tile[part * kTok + t][g];
+    const uint32_t w = tile[part * kTok + t][g];
     if constexpr (kCh == 2) {
-      amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(w[t] << 16)));
-      amax[1] = fmaxf(amax[1], fabsf(__uint_as_float(w[t] & 0xFFFF0000u)));
+      amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(w << 16)));
+      amax[1] = fmaxf(amax[1], fabsf(__uint_as_float(w & 0xFFFF0000u)));
     } else {
-      amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(w[t])));
+      amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(w)));
     }
   }
 #pragma unroll
@@ -238,15 +237,15 @@ __global__ void __launch_bounds__(256, 4) quant_128x1_kernel(const TIn* __restri
     const int64_t c = c0 + g * kCh + k;
     if (c < C) {
       uint8_t* dst = qT + c * ldq + tb * 128 + part * kTok;
-#pragma unroll
-      for (int t = 0; t < kTok; t += 16) {
+#pragma unroll 1
+      for (int t = 0; t < kTok; t += 16) {   // words re-read from shared memory (no spills)
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float f[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint32_t wv = w[t + 4 * j + i];
+            const uint32_t wv = tile[part * kTok + t + 4 * j + i][g];
             f[i] = __uint_as_float(kCh == 1 ? wv : (k == 0 ? (wv << 16) : (wv & 0xFFFF0000u)));
           }
           o[j] = e4m3x4(f, r);
@@ -364,6 +363,138 @@ __global__ void __launch_bounds__(256, 5) quant_128x128_kernel(const TIn* __rest
         *reinterpret_cast<uint32_t*>(d) = e4m3x4(f, r);
       }
     }
+  }
+}
+
+// ------------------------------------------------------------ dual 1x128 + 128x1
+// One read of a 128-token x 128-channel block of X gives both granularities the
+// layer step needs: the 1x128 codes (row-major, the A operand of Fprop / Dgrad)
+// and the 128x1 codes (transposed, the operand of Wgrad), each bit-identical to
+// the single-granularity kernels.  The block is staged in shared memory with
+// cp.async; its 16-byte chunks are XOR-swizzled by row (chunk ^ (row & 7)) so
+// that both the row pass (4 lanes per row, 8 rows per warp) and the column
+// pass (32 consecutive words of one row per warp) read without bank conflicts.
+template <typename TIn>
+__global__ void __launch_bounds__(256) quant_dual_kernel(const TIn* __restrict__ x, int64_t ldx,
+                                                         uint8_t* __restrict__ q, int64_t ldq,
+                                                         float* __restrict__ s, int64_t lds,
+                                                         uint8_t* __restrict__ qT, int64_t ldqT,
+                                                         float* __restrict__ sT, int64_t ldsT) {
+  constexpr int kVec = Vec16<TIn>::kN;                      // elements per 16 bytes
+  constexpr int kChunksPerRow = 128 / kVec;                 // 16 (bf16) or 32 (fp32)
+  constexpr int kWordsPerRow = kChunksPerRow * 4;
+  constexpr int kCh = 4 / sizeof(TIn);                      // channels per 32-bit word
+  constexpr int kParts = 256 / kWordsPerRow;                // 4 or 2 token parts
+  constexpr int kRows = 128 / kParts;                       // 32 or 64 tokens per thread
+  extern __shared__ __align__(16) unsigned char dual_smem[];
+  uint32_t* tile = reinterpret_cast<uint32_t*>(dual_smem);  // [128][kWordsPerRow], swizzled
+  __shared__ float part_amax[kParts][128];
+
+  const int64_t tb = blockIdx.y, cb = blockIdx.x;
+  const int tid = threadIdx.x;
+  auto chunk_at = [](int row, int chunk) { return row * kChunksPerRow + (chunk ^ (row & 7)); };
+  {
+    const TIn* src = x + tb * 128 * ldx + cb * 128;
+#pragma unroll 4
+    for (int i = tid; i < 128 * kChunksPerRow; i += 256) {
+      const int row = i / kChunksPerRow, ch = i % kChunksPerRow;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                       smem_u32(tile + chunk_at(row, ch) * 4)),
+                   "l"(src + row * ldx + ch * kVec)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  }
+  __syncthreads();
+
+  // ---- 1x128: four lanes per token row; load i of lane l is chunk i*4 + l
+  {
+    const int warp = tid >> 5, lane = tid & 31;
+    const int l = lane & 3;
+    constexpr int kLoads = kChunksPerRow / 4;
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int row = warp * 16 + pass * 8 + (lane >> 2);
+      uint4 v[kLoads];
+#pragma unroll
+      for (int i = 0; i < kLoads; ++i)
+        v[i] = *reinterpret_cast<const uint4*>(tile + chunk_at(row, i * 4 + l) * 4);
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kLoads; ++i) {
+        float f[kVec];
+        Vec16<TIn>::widen(v[i], f);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) amax = fmaxf(amax, fabsf(f[j]));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      float sc, r;
+      tile_scale(amax, sc, r);
+      uint8_t* dst = q + (tb * 128 + row) * ldq + cb * 128 + l * kVec;
+#pragma unroll
+      for (int i = 0; i < kLoads; ++i) {
+        float f[kVec];
+        Vec16<TIn>::widen(v[i], f);
+        if constexpr (kVec == 8) {
+          *reinterpret_cast<uint2*>(dst + i * 4 * kVec) = make_uint2(e4m3x4(f, r), e4m3x4(f + 4, r));
+        } else {
+          *reinterpret_cast<uint32_t*>(dst + i * 4 * kVec) = e4m3x4(f, r);
+        }
+      }
+      if (l == 0) s[cb * lds + tb * 128 + row] = sc;
+    }
+  }
+
+  // ---- 128x1: thread (g, part) owns word column g over its run of token rows
+  const int g = tid % kWordsPerRow;
+  const int part = tid / kWordsPerRow;
+  auto word_at = [&](int row) {
+    return tile[chunk_at(row, g >> 2) * 4 + (g & 3)];
+  };
+  {
+    float amax[kCh];
+#pragma unroll
+    for (int k = 0; k < kCh; ++k) amax[k] = 0.0f;
+#pragma unroll 8
+    for (int t = 0; t < kRows; ++t) {
+      const uint32_t w = word_at(part * kRows + t);
+      if constexpr (kCh == 2) {
+        amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(w << 16)));
+        amax[1] = fmaxf(amax[1], fabsf(__uint_as_float(w & 0xFFFF0000u)));
+      } else {
+        amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(w)));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kCh; ++k) part_amax[part][g * kCh + k] = amax[k];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kCh; ++k) {
+    const int c = g * kCh + k;
+    float a = part_amax[0][c];
+#pragma unroll
+    for (int p2 = 1; p2 < kParts; ++p2) a = fmaxf(a, part_amax[p2][c]);
+    float sc, r;
+    tile_scale(a, sc, r);
+    uint8_t* dst = qT + (cb * 128 + c) * ldqT + tb * 128 + part * kRows;
+#pragma unroll 1
+    for (int t = 0; t < kRows; t += 16) {
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float f[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t wv = word_at(part * kRows + t + 4 * j + i);
+          f[i] = __uint_as_float(kCh == 1 ? wv : (k == 0 ? (wv << 16) : (wv & 0xFFFF0000u)));
+        }
+        o[j] = e4m3x4(f, r);
+      }
+      *reinterpret_cast<uint4*>(dst + t) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (part == 0) sT[tb * ldsT + cb * 128 + c] = sc;
   }
 }
 

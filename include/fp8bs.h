@@ -102,6 +102,24 @@ fp8bs_status fp8bs_quant_act_128x1(const void* x, fp8bs_dtype xt, int64_t T, int
                                    int64_t ldx, uint8_t* qT, int64_t ldq, float* s,
                                    int64_t lds, void* stream);
 
+/* Both activation quantizers in one pass over x (the backward pass needs the
+ * 1x128 codes for Dgrad's A operand and the 128x1 codes for Wgrad, and the
+ * pages keep activations in FP8 for it): x is read once and
+ *   q, s    receive exactly what fp8bs_quant_act_1x128(x, ...) writes
+ *           (q [T x C] row-major, ldq >= C; s[cb*lds + t], lds >= T);
+ *   qT, sT  receive exactly what fp8bs_quant_act_128x1(x, ...) writes
+ *           (qT [C x T], ldqT >= T; sT[tb*ldsT + c], ldsT >= C).
+ * Source: "Should Fixing Deepseek Take 60 Steps?", Figure 6 and Figure 7 (a)
+ * passages; untitled page at jp-study.kr, Figure 6 passage (FP8 activations
+ * cached for the backward pass).
+ * Requirements: T % 128 == 0 and C % 128 == 0 (UNSUPPORTED); x, q, qT 16-byte
+ * aligned, ldx*sizeof(xt), ldq, ldqT multiples of 16; s, sT 4-byte aligned
+ * (MISALIGNED).  T == 0 or C == 0 is a no-op. */
+fp8bs_status fp8bs_quant_act_dual(const void* x, fp8bs_dtype xt, int64_t T, int64_t C,
+                                  int64_t ldx, uint8_t* q, int64_t ldq, float* s, int64_t lds,
+                                  uint8_t* qT, int64_t ldqT, float* sT, int64_t ldsT,
+                                  void* stream);
+
 /* 128x128 weight quantizer (one scale per 128 x 128 block).
  *   w  [R x C] fp32 or bf16, row stride ldw >= C.
  *   q  [R x C] E4M3 codes (ldq >= C) -- may be NULL;
@@ -159,6 +177,21 @@ fp8bs_status fp8bs_gemm_ws(int64_t M, int64_t N, int64_t K,
                            const uint8_t* B, int64_t ldb, const float* sb, fp8bs_bscale sb_mode,
                            int64_t ldsb, void* C, fp8bs_dtype ct, int64_t ldc, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/* Accumulating GEMM for FP32 gradients:  C[M x N] += A[M x K] * B[N x K]^T,
+ * C fp32 (the Wgrad of several micro-batches summed into one FP32 gradient;
+ * the pages keep gradients in FP32: untitled page at jp-study.kr, FP32 master
+ * weights and gradients passage).  Each output element receives the block-
+ * scaled product computed as in fp8bs_gemm, added once to its previous value
+ * (whole tiles: TMA reduce-add in L2; tiles of a split last wave: by the
+ * partial-sum kernel).  workspace / workspace_bytes as in fp8bs_gemm_ws
+ * (NULL: no split).  K == 0 leaves C unchanged.  Other arguments,
+ * requirements and errors are those of fp8bs_gemm with ct = FP8BS_F32. */
+fp8bs_status fp8bs_gemm_accumulate(int64_t M, int64_t N, int64_t K,
+                                   const uint8_t* A, int64_t lda, const float* sa, int64_t ldsa,
+                                   const uint8_t* B, int64_t ldb, const float* sb,
+                                   fp8bs_bscale sb_mode, int64_t ldsb, float* C, int64_t ldc,
+                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* fp8bs_gemm_ws for callers that cannot allocate device memory: some cannot
  * call cudaMalloc at all where they run (e.g. code that may not synchronize

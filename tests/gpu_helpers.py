@@ -39,6 +39,21 @@ def gpu_quant_128x1(x: torch.Tensor):
     return qT.cpu().numpy(), s.cpu().numpy()
 
 
+def gpu_quant_dual(x: torch.Tensor, pad: int = 0):
+    """Both activation quantizers from one pass; outputs padded by `pad`
+    elements in every leading dimension (pre-filled with sentinels)."""
+    T, C = x.shape
+    xd = torch.zeros((T, C + pad * 8), dtype=x.dtype, device=DEV)[:, :C]
+    xd.copy_(x)
+    q = torch.full((T, C + pad * 16), 0xAB, dtype=torch.uint8, device=DEV)[:, :C]
+    s = torch.full((C // 128, T + pad), -1.0, dtype=torch.float32, device=DEV)[:, :T]
+    qT = torch.full((C, T + pad * 16), 0xAB, dtype=torch.uint8, device=DEV)[:, :T]
+    sT = torch.full((T // 128, C + pad), -1.0, dtype=torch.float32, device=DEV)[:, :C]
+    fb.fp8bs_quant_act_dual(xd, q, s, qT, sT)
+    assert fb.fp8bs_sync_status() == fb.FP8BS_OK
+    return q.cpu().numpy(), s.cpu().numpy(), qT.cpu().numpy(), sT.cpu().numpy()
+
+
 def gpu_quant_w(w: torch.Tensor, want_q: bool = True, want_qT: bool = True):
     R, C = w.shape
     wd = w.to(DEV)

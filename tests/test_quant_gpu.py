@@ -7,7 +7,8 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_helpers import gpu_quant_1x128, gpu_quant_128x1, gpu_quant_w, oracle_input
+from gpu_helpers import (gpu_quant_1x128, gpu_quant_128x1, gpu_quant_dual, gpu_quant_w,
+                         oracle_input)
 
 pytestmark = pytest.mark.gpu
 
@@ -168,3 +169,38 @@ def test_quant_layer_weight_full():
     _eq(s, sr, "scales")
     _eq(q, qr, "codes")
     _eq(qT, qTr, "transposed codes")
+
+
+def _check_dual(x, what, pad=0):
+    q, s, qT, sT = gpu_quant_dual(x, pad=pad)
+    qr, sr = oracle.quant_act_1x128(oracle_input(x))
+    qTr, sTr = oracle.quant_act_128x1(oracle_input(x))
+    _eq(q, qr, f"{what}: 1x128 codes")
+    _eq(s, sr, f"{what}: 1x128 scales")
+    _eq(qT, qTr, f"{what}: 128x1 codes")
+    _eq(sT, sTr, f"{what}: 128x1 scales")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("T,C", [(128, 128), (256, 640), (384, 1152), (512, 7168)])
+def test_quant_dual_matches_oracle(dtype, T, C):
+    """One pass gives exactly the 1x128 and the 128x1 quantizers' outputs."""
+    x = wl.random_matrix((T, C), seed=T * 5 + C, dtype=dtype)
+    _check_dual(x, f"{T}x{C} {dtype}")
+
+
+def test_quant_dual_padded_strides_and_edge_blocks():
+    x = np.zeros((256, 512), np.float32)
+    x[0:128, 0:128] = 0.0                         # all-zero block: s = 1 both ways
+    x[0:128, 128:256] = 1e-37                     # amax too small for 448/amax
+    x[128:256, 256:384] = np.float32(3.0e38)      # huge
+    x[5, 300] = -7.0
+    x[128:, 384:] = np.linspace(-2.0, 3.0, 128 * 128, dtype=np.float32).reshape(128, 128)
+    for dtype in (torch.float32, torch.bfloat16):
+        _check_dual(torch.from_numpy(x).to(dtype), f"edges {dtype}", pad=3)
+
+
+def test_quant_dual_layer_activations_and_grads():
+    """The layer step's two activation tensors, in full."""
+    _check_dual(wl.layer_activations(), "X 4096x7168")
+    _check_dual(wl.layer_grad_output(), "dY 4096x18432")
