@@ -56,7 +56,11 @@ def dual_bytes(elems: int, in_bytes: int) -> float:
 
 # DRAM traffic per launch measured by ncu (dram__bytes_read.sum + write.sum), with
 # the sha256 of the kernel source it was measured on; ignored once the source changes.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # ncu --set full, one launch of `bench.py --case wgrad` (profiles/gemm_pair_layer_ncu_full.md)
+    "gemm_wgrad": {"file": "gemm_pair_kernel.cuh", "src": "a5472a50fd78df0d",
+                   "bytes": 192056064 + 496465664},
+}
 
 
 def _src_hash(name: str) -> str:
@@ -294,41 +298,67 @@ def run_fp8bs(args, rank, world, dist_on):
 
 
 def run_e2e(step, x_h, w_h, dy_h, dev, stream, args, dist_on, world):
-    """The same step from pinned host buffers: H2D of X, W, dY, the eight
-    library calls, D2H of Y, dX, dW, all inside the timed region."""
+    """The same step through the same entry points from pinned host buffers,
+    copies included: every step uploads X, W, dY and downloads Y, dX, dW.
+    The copies are pipelined against the compute on three streams with two
+    device buffer sets (upload of step i+1 and download of step i-1 overlap
+    the compute of step i; PCIe carries both directions at once)."""
     xp, wp, dyp = x_h.pin_memory(), w_h.pin_memory(), dy_h.pin_memory()
-    Yh = torch.empty(step.Y.shape, dtype=step.Y.dtype).pin_memory()
-    dXh = torch.empty(step.dX.shape, dtype=step.dX.dtype).pin_memory()
-    dWh = torch.empty(step.dW.shape, dtype=step.dW.dtype).pin_memory()
-    fns = step.launches()
+    sets = [step, LayerStep(torch.empty_like(step.x), torch.empty_like(step.w),
+                            torch.empty_like(step.dy), dev)]
+    outs = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (st.Y, st.dX, st.dW))
+            for st in sets]
+    fns = [st.launches() for st in sets]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    comp_done, out_done = {}, {}
 
-    def one():
-        step.x.copy_(xp, non_blocking=True)
-        step.w.copy_(wp, non_blocking=True)
-        step.dy.copy_(dyp, non_blocking=True)
-        for f in fns:
+    def one(i):
+        b = i % 2
+        st = sets[b]
+        if i >= 2:   # buffer set b is free once step i-2 computed and was read back
+            s_in.wait_event(comp_done[i - 2])
+        with torch.cuda.stream(s_in):
+            st.x.copy_(xp, non_blocking=True)
+            st.w.copy_(wp, non_blocking=True)
+            st.dy.copy_(dyp, non_blocking=True)
+            in_done = torch.cuda.Event()
+            in_done.record(s_in)
+        stream.wait_event(in_done)
+        if i >= 2:
+            stream.wait_event(out_done[i - 2])
+        for f in fns[b]:
             f(stream)
-        Yh.copy_(step.Y, non_blocking=True)
-        dXh.copy_(step.dX, non_blocking=True)
-        dWh.copy_(step.dW, non_blocking=True)
+        comp_done[i] = torch.cuda.Event()
+        comp_done[i].record(stream)
+        s_out.wait_event(comp_done[i])
+        with torch.cuda.stream(s_out):
+            for h, d in zip(outs[b], (st.Y, st.dX, st.dW)):
+                h.copy_(d, non_blocking=True)
+            out_done[i] = torch.cuda.Event()
+            out_done[i].record(s_out)
 
-    for _ in range(2):
-        one()
+    for i in range(2):
+        one(i)
     torch.cuda.synchronize(dev)
-    n = max(2, min(args.steps, 5))
+    n = max(4, min(args.steps, 8))
     _barrier(dist_on)
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(n):
-        one()
-    e.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for i in range(2, 2 + n):
+        one(i)
+    s_in.wait_stream(s_out)
+    t1.record(s_in)
     torch.cuda.synchronize(dev)
     _barrier(dist_on)
-    ms = _max_over_ranks(s.elapsed_time(e) / n, dist_on)
+    ms = _max_over_ranks(t0.elapsed_time(t1) / n, dist_on)
     h2d = sum(t.numel() * t.element_size() for t in (xp, wp, dyp))
-    d2h = sum(t.numel() * t.element_size() for t in (Yh, dXh, dWh))
+    d2h = sum(t.numel() * t.element_size() for t in outs[0])
+    if step.fb.fp8bs_sync_status(stream) != 0:
+        raise RuntimeError("device error during the end-to-end run")
     return {"value": round(world * 3 * GEMM_FLOPS / (ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
-            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelining": "H2D / compute / D2H on three streams, two device buffer sets",
+            "steps": n}
 
 
 def run_extras(dev, stream, peaks):
