@@ -70,10 +70,12 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_status_string.argtypes = [I]
         L.fp8bs_status_string.restype = ctypes.c_char_p
         L.fp8bs_debug_timeout_probe.argtypes = [I64, P]
+        L.fp8bs_probe_mma_f8f6f4.argtypes = [P, P, I64, P, P]
         for name in ("fp8bs_quant_act_1x128", "fp8bs_quant_act_128x1", "fp8bs_quant_w_128x128",
                      "fp8bs_gemm", "fp8bs_grouped_gemm", "fp8bs_sync_status",
                      "fp8bs_debug_timeout_probe", "fp8bs_gemm_workspace_size", "fp8bs_gemm_ws",
-                     "fp8bs_gemm_static_ws", "fp8bs_quant_act_dual", "fp8bs_gemm_accumulate"):
+                     "fp8bs_gemm_static_ws", "fp8bs_quant_act_dual", "fp8bs_gemm_accumulate",
+                     "fp8bs_probe_mma_f8f6f4"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -239,6 +241,14 @@ def fp8bs_grouped_gemm(offsets, A, sa, B, sb, sb_mode: int, C, stream=None):
 def fp8bs_sync_status(stream=None) -> int:
     """Synchronize and return (and clear) the device error status."""
     return lib().fp8bs_sync_status(_stream(stream))
+
+
+def fp8bs_probe_mma_f8f6f4(a, b, d, stream=None):
+    """d [128 x 256] fp32 = a [128 x K] * b [256 x K]^T over raw E4M3 codes,
+    as the tensor cores compute it (K in 32..128, multiple of 32)."""
+    K = a.shape[1]
+    _check(lib().fp8bs_probe_mma_f8f6f4(_ptr(a), _ptr(b), K, _ptr(d), _stream(stream)),
+           "fp8bs_probe_mma_f8f6f4")
 
 
 def fp8bs_debug_timeout_probe(limit_ns: int, stream=None):

@@ -653,6 +653,19 @@ const char* fp8bs_status_string(fp8bs_status status) {
   return "unknown status";
 }
 
+fp8bs_status fp8bs_probe_mma_f8f6f4(const uint8_t* a, const uint8_t* b, int64_t K, float* d,
+                                    void* stream) {
+  if (a == nullptr || b == nullptr || d == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (K < 32 || K > 128 || K % 32 != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (!aligned(d, 4)) return FP8BS_ERR_MISALIGNED;
+  if (cudaFuncSetAttribute(fp8bs_mma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kProbeSmemBytes)) != cudaSuccess)
+    return FP8BS_ERR_CUDA;
+  fp8bs_mma_probe_kernel<<<1, 128, kProbeSmemBytes, as_stream(stream)>>>(a, b, static_cast<int>(K),
+                                                                         d);
+  return launch_status();
+}
+
 fp8bs_status fp8bs_debug_timeout_probe(int64_t limit_ns, void* stream) {
   if (limit_ns < 1000 || limit_ns > 10000000000LL) return FP8BS_ERR_INVALID_ARG;
   fp8bs_timeout_probe_kernel<<<1, 32, 0, as_stream(stream)>>>(static_cast<uint64_t>(limit_ns));

@@ -471,6 +471,79 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 #undef FP8BS_NUM_TILES
 
+constexpr size_t kProbeSmemBytes = 1024 + (128 + 256) * 128;   // alignment slack + A + B
+
+// Accumulation probe: D[128][256] = A[128][K] * B[256][K]^T over raw E4M3
+// codes (no scales), K = 32 * n_mma <= 128, with n_mma tcgen05 kind::f8f6f4
+// MMAs (M=128, N=256, K=32) accumulating in TMEM, read back as raw FP32.  The
+// operands are copied into shared memory in the 128-byte-swizzled K-major
+// layout the MMA descriptors describe (row r's 16-byte chunk j at chunk
+// position j ^ (r & 7)); bytes past K are zero.  One CTA of 128 threads.
+__global__ void __launch_bounds__(128, 1) fp8bs_mma_probe_kernel(const uint8_t* __restrict__ a,
+                                                                 const uint8_t* __restrict__ b,
+                                                                 int K, float* __restrict__ d) {
+  extern __shared__ __align__(1024) unsigned char probe_smem_raw[];   // kProbeSmemBytes
+  unsigned char* op = probe_smem_raw + ((1024u - (smem_u32(probe_smem_raw) & 1023u)) & 1023u);
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < (128 + 256) * 8; i += 128) {   // 16-byte chunks
+    const int r = i / 8, j = i % 8;
+    const uint8_t* src = r < 128 ? a + static_cast<int64_t>(r) * K : b + static_cast<int64_t>(r - 128) * K;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int k = j * 16 + q * 4 + t;
+        if (k < K) v |= static_cast<uint32_t>(src[k]) << (8 * t);
+      }
+      w[q] = v;
+    }
+    const int rr = r < 128 ? r : r - 128;
+    unsigned char* base = op + (r < 128 ? 0 : 128 * 128);
+    *reinterpret_cast<uint4*>(base + rr * 128 + ((j ^ (rr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    abort_s = 0;
+    fence_mbarrier_init();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (warp == 0) tmem_alloc(&tmem_base_s, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base_s;
+  if (tid == 0) {
+    const uint64_t adesc = smem_desc_k_sw128(smem_u32(op));
+    const uint64_t bdesc = smem_desc_k_sw128(smem_u32(op + 128 * 128));
+    for (int kk = 0; kk < K / 32; ++kk)
+      mma_f8f6f4(tb, adesc + 2u * kk, bdesc + 2u * kk, idesc_e4m3_f32(128, 256), kk > 0 ? 1u : 0u);
+    mma_commit(&bar);
+  }
+  __syncwarp();
+  const bool ok = bounded_wait(&bar, 0, &abort_s);
+  tc_fence_after();
+  if (ok) {
+    uint32_t r[32];
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+      tmem_ld32(tb + (static_cast<uint32_t>(warp * 32) << 16) + c, r);
+      tmem_wait_ld(r);
+      float* row = d + static_cast<int64_t>(warp * 32 + lane) * 256 + c;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) row[i] = __uint_as_float(r[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tb, 256);
+}
+
 // One CTA waits on a barrier that nothing arrives at, with a time limit; the
 // wait gives up, records a timeout in the device error word and returns.
 __global__ void fp8bs_timeout_probe_kernel(uint64_t limit_ns) {

@@ -243,6 +243,20 @@ fp8bs_status fp8bs_sync_status(void* stream);
 /* Static string naming a status code. */
 const char* fp8bs_status_string(fp8bs_status status);
 
+/* Accumulation probe of the tensor cores (the page at why-be.why-be.co.kr,
+ * accumulation-precision passage: on H800 the FP8 MMA keeps only about 14
+ * bits of its accumulated sum).  Computes D[128][256] = A[128][K] * B[256][K]^T
+ * over raw E4M3 codes (no scales) with K/32 tcgen05 kind::f8f6f4 MMAs
+ * (M=128, N=256, K=32) accumulating in TMEM, and returns the FP32 result as
+ * the hardware produced it, so the caller can compare it with the exact sum.
+ *   a  [128][K] codes, row stride K bytes (device);  b [256][K] likewise;
+ *   d  [128][256] fp32, row-major (device).
+ * Requirements: K in {32, 64, 96, 128} (UNSUPPORTED); pointers non-NULL
+ * (INVALID_ARG), d 4-byte aligned (MISALIGNED).  One CTA; asynchronous on
+ * the stream; fp8bs_sync_status reports a device-side timeout. */
+fp8bs_status fp8bs_probe_mma_f8f6f4(const uint8_t* a, const uint8_t* b, int64_t K, float* d,
+                                    void* stream);
+
 /* Test hook for the failure path: launch one CTA that waits on a barrier no
  * one arrives at, with a limit of limit_ns nanoseconds (1e3 .. 1e10).  The
  * wait gives up, records a timeout in the device error word and returns, so
