@@ -83,7 +83,7 @@ int pair_clusters(K kernel) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 512, 1, 1);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
-    cfg.dynamicSmemBytes = kPairSmemBytes;
+    cfg.dynamicSmemBytes = pair_smem_bytes<256>();
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
@@ -212,9 +212,9 @@ fp8bs_status check_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
 // Co-resident 2-CTA clusters of the pair GEMM on the current device (all its
 // variants have the same shape and resources).
 fp8bs_status pair_cluster_count(int* clusters) {
-  auto kernel = fp8bs_gemm_pair_kernel<kSbBlock, true>;
+  auto kernel = fp8bs_gemm_pair_kernel<256, kSbBlock, true>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kPairSmemBytes)) != cudaSuccess)
+                           static_cast<int>(pair_smem_bytes<256>())) != cudaSuccess)
     return FP8BS_ERR_CUDA;
   *clusters = pair_clusters(kernel);
   return *clusters > 0 ? FP8BS_OK : FP8BS_ERR_CUDA;
@@ -229,9 +229,15 @@ struct SplitPlan {
   size_t ws_bytes;
 };
 constexpr int kMaxSplits = 32;
-constexpr size_t kPartialTileBytes = static_cast<size_t>(kPairTileM) * kBN * sizeof(float);
 
-SplitPlan plan_split(int tiles, int KB, int clusters, size_t ws_avail) {
+// Tile width of the pair GEMM.  256 for every mode: measured on the layer's
+// GEMMs, the 128-wide tile (four TMEM buffers, 45 % more operand bytes per
+// FLOP) was slower everywhere (Fprop 0.42 -> 0.69 ms, Dgrad 0.53 -> 1.05 ms,
+// Wgrad 0.62 -> 0.89 ms), so the kernel's BN = 128 form is not instantiated.
+int pair_tile_n(fp8bs_bscale /*mode*/) { return 256; }
+
+SplitPlan plan_split(int tiles, int KB, int clusters, size_t ws_avail, int bn) {
+  const size_t kPartialTileBytes = static_cast<size_t>(kPairTileM) * bn * sizeof(float);
   SplitPlan sp{tiles, 1, tiles, 0, 0};
   if (tiles <= 0 || clusters <= 0) return sp;
   const int tail = tiles % clusters;
@@ -251,36 +257,38 @@ SplitPlan plan_split(int tiles, int KB, int clusters, size_t ws_avail) {
   return sp;
 }
 
+template <int BN>
 fp8bs_status launch_gemm_pair(GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& tc, const CUtensorMap& tws, const float* ws,
                               int tail, int clusters, int sb_kind, fp8bs_dtype ct, bool acc,
                               cudaStream_t stream) {
+  constexpr size_t smem = pair_smem_bytes<BN>();
   auto run = [&](auto kernel) -> fp8bs_status {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kPairSmemBytes)) != cudaSuccess)
+                             static_cast<int>(smem)) != cudaSuccess)
       return FP8BS_ERR_CUDA;
     const int grid_clusters = p.units < clusters ? p.units : clusters;
-    kernel<<<2 * grid_clusters, kGemmThreads, kPairSmemBytes, stream>>>(p, ta, tb, tc, tws);
+    kernel<<<2 * grid_clusters, kGemmThreads, smem, stream>>>(p, ta, tb, tc, tws);
     fp8bs_status st = launch_status();
     if (st != FP8BS_OK || tail == 0) return st;
-    const unsigned blocks = static_cast<unsigned>(tail) * (kPairTileM * 64 / 256);
+    const unsigned blocks = static_cast<unsigned>(tail) * (kPairTileM * (BN / 4) / 256);
     if (ct == FP8BS_BF16)
-      split_fixup_kernel<true><<<blocks, 256, 0, stream>>>(ws, p, tail);
+      split_fixup_kernel<BN, true><<<blocks, 256, 0, stream>>>(ws, p, tail);
     else if (acc)
-      split_fixup_kernel<false, true><<<blocks, 256, 0, stream>>>(ws, p, tail);
+      split_fixup_kernel<BN, false, true><<<blocks, 256, 0, stream>>>(ws, p, tail);
     else
-      split_fixup_kernel<false><<<blocks, 256, 0, stream>>>(ws, p, tail);
+      split_fixup_kernel<BN, false><<<blocks, 256, 0, stream>>>(ws, p, tail);
     return launch_status();
   };
   const bool bf16 = ct == FP8BS_BF16;
   if (acc)   // FP32 output only
-    return sb_kind == kSbBlock ? run(fp8bs_gemm_pair_kernel<kSbBlock, false, true>)
-                               : run(fp8bs_gemm_pair_kernel<kSbPerCol, false, true>);
+    return sb_kind == kSbBlock ? run(fp8bs_gemm_pair_kernel<BN, kSbBlock, false, true>)
+                               : run(fp8bs_gemm_pair_kernel<BN, kSbPerCol, false, true>);
   if (sb_kind == kSbBlock)
-    return bf16 ? run(fp8bs_gemm_pair_kernel<kSbBlock, true>)
-                : run(fp8bs_gemm_pair_kernel<kSbBlock, false>);
-  return bf16 ? run(fp8bs_gemm_pair_kernel<kSbPerCol, true>)
-              : run(fp8bs_gemm_pair_kernel<kSbPerCol, false>);
+    return bf16 ? run(fp8bs_gemm_pair_kernel<BN, kSbBlock, true>)
+                : run(fp8bs_gemm_pair_kernel<BN, kSbBlock, false>);
+  return bf16 ? run(fp8bs_gemm_pair_kernel<BN, kSbPerCol, true>)
+              : run(fp8bs_gemm_pair_kernel<BN, kSbPerCol, false>);
 }
 
 template <bool kGrouped>
@@ -378,16 +386,17 @@ fp8bs_status gemm_dense(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
   fp8bs_status st = check_gemm(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc);
   if (st != FP8BS_OK || M == 0 || N == 0) return st;
   if (K == 0) return acc ? FP8BS_OK : zero_fill(C, ct, M, N, ldc, as_stream(stream));
+  const int bn = pair_tile_n(sb_mode);
   CUtensorMap ta, tb, tc;
   if ((st = make_map_2d(&ta, A, K, M, lda, kBM)) != FP8BS_OK) return st;
-  if ((st = make_map_2d(&tb, B, K, N, ldb, kBN / 2)) != FP8BS_OK) return st;
+  if ((st = make_map_2d(&tb, B, K, N, ldb, bn / 2)) != FP8BS_OK) return st;
   if ((st = make_map_out(&tc, C, ct, N, M, ldc)) != FP8BS_OK) return st;
   GemmParams p{};
   p.M = static_cast<int32_t>(M);
   p.N = static_cast<int32_t>(N);
   p.KB = static_cast<int32_t>(K / kBK);
   p.num_m_tiles = static_cast<int32_t>((M + kPairTileM - 1) / kPairTileM);
-  p.num_n_tiles = static_cast<int32_t>((N + kBN - 1) / kBN);
+  p.num_n_tiles = static_cast<int32_t>((N + bn - 1) / bn);
   p.E = 1;
   p.sa = sa;
   p.ldsa = ldsa;
@@ -400,18 +409,18 @@ fp8bs_status gemm_dense(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
   int clusters = 0;
   if ((st = pair_cluster_count(&clusters)) != FP8BS_OK) return st;
   const SplitPlan sp = plan_split(p.num_m_tiles * p.num_n_tiles, p.KB, clusters,
-                                  ws != nullptr ? ws_bytes : 0);
+                                  ws != nullptr ? ws_bytes : 0, bn);
   p.full_tiles = sp.full_tiles;
   p.splits = sp.splits;
   p.units = sp.units;
   CUtensorMap tws = tc;   // unused without a split
   if (sp.tail > 0 &&
-      (st = make_map_out(&tws, ws, FP8BS_F32, kBN,
-                         static_cast<uint64_t>(sp.tail) * sp.splits * kPairTileM, kBN)) != FP8BS_OK)
+      (st = make_map_out(&tws, ws, FP8BS_F32, bn,
+                         static_cast<uint64_t>(sp.tail) * sp.splits * kPairTileM, bn)) != FP8BS_OK)
     return st;
-  return launch_gemm_pair(p, ta, tb, tc, tws, ws, sp.tail, clusters,
-                          sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct, acc,
-                          as_stream(stream));
+  const int sb_kind = sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock;
+  return launch_gemm_pair<256>(p, ta, tb, tc, tws, ws, sp.tail, clusters, sb_kind, ct, acc,
+                               as_stream(stream));
 }
 
 }  // namespace
@@ -547,9 +556,13 @@ fp8bs_status fp8bs_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* 
   int clusters = 0;
   fp8bs_status st = pair_cluster_count(&clusters);
   if (st != FP8BS_OK) return st;
-  const int64_t tiles = ((M + kPairTileM - 1) / kPairTileM) * ((N + kBN - 1) / kBN);
-  if (tiles > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
-  *bytes = plan_split(static_cast<int>(tiles), static_cast<int>(K / kBK), clusters, SIZE_MAX).ws_bytes;
+  for (int bn : {256}) {
+    const int64_t tiles = ((M + kPairTileM - 1) / kPairTileM) * ((N + bn - 1) / bn);
+    if (tiles > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+    const size_t need =
+        plan_split(static_cast<int>(tiles), static_cast<int>(K / kBK), clusters, SIZE_MAX, bn).ws_bytes;
+    if (need > *bytes) *bytes = need;
+  }
   return FP8BS_OK;
 }
 

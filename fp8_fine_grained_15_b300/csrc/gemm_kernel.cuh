@@ -159,16 +159,17 @@ __device__ __forceinline__ void promote32_percol(float2* acc, const uint32_t (&r
   }
 }
 
-// Store this warp's 32 rows x 128 accumulator columns (row `lane` per
+// Store this warp's 32 rows x kCols accumulator columns (row `lane` per
 // thread) through a 2 KB shared buffer and 64-byte-wide TMA boxes at (col, row)
 // of `tmap`: FP32 (16 columns per box) or BF16 rounded to nearest even (32).
-// kAdd: the FP32 boxes are added into the existing values instead.
-template <bool kBf16, bool kAdd = false>
+// kAdd: the FP32 boxes are added into the existing values instead.  kCols:
+// accumulator columns of the warp (128, or 64 for the 128-wide pair tile).
+template <bool kBf16, bool kAdd = false, int kCols = 128>
 __device__ __forceinline__ void store_rows_tma(const float2* acc, uint32_t stg, int lane,
                                                const CUtensorMap* tmap, int col, int row) {
   constexpr int kChunkCols = kBf16 ? 32 : 16;   // 64 bytes of output per row
 #pragma unroll
-  for (int c = 0; c < 128 / kChunkCols; ++c) {
+  for (int c = 0; c < kCols / kChunkCols; ++c) {
     // the previous bulk store of this buffer must have read it
     if (lane == 0) bulk_wait_read_all();
     __syncwarp();

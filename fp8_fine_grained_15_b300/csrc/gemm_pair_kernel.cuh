@@ -10,9 +10,15 @@
 // Why pairs: with one CTA per 128x256 tile each SM pulls 48 KB of operands per
 // slab from L2 and only four such stages fit in shared memory; measured, the
 // TMA round trip (~2900 cycles at that load) then bounds the slab rate.  A
-// cluster of two CTAs computes a 256x256 tile with one pair MMA: each CTA
-// stages its own 128 rows of A and one half (128 rows) of B, so an SM pulls
-// 32 KB per slab and six stages fit.
+// cluster of two CTAs computes a 256 x BN tile with one pair MMA: each CTA
+// stages its own 128 rows of A and one half (BN/2 rows) of B.
+//
+// Tile width BN: 256 (32 KB per SM and slab, 6 stages, two 256-column TMEM
+// slab buffers) is what the library launches.  BN = 128 (24 KB, 8 stages, four
+// 128-column buffers) compiles and passes the parity tests; pair MMAs with
+// N = 128 stream at 97 % of the N = 256 rate in isolation, but with 45 % more
+// operand bytes per FLOP the whole kernel measured 1.4-2x slower on the
+// layer's GEMMs, so it is not instantiated.
 //
 // Roles (384 threads per CTA, both CTAs of the pair):
 //   warp 0      TMA producer: this CTA's A rows and B half of each slab; the
@@ -34,11 +40,20 @@
 
 namespace fp8bs {
 
-constexpr int kPairStages = 6;
-constexpr int kPairStageA = kBM * kBK;          // this CTA's 128 rows of A, one slab
-constexpr int kPairStageB = (kBN / 2) * kBK;    // this CTA's half of the B tile
-constexpr int kPairStageBytes = kPairStageA + kPairStageB;
 constexpr int kPairTileM = 2 * kBM;             // rows of a pair tile
+constexpr int kPairRingBytes = 6 * 32768;       // operand ring per CTA
+
+template <int BN>
+struct PairCfg {
+  static_assert(BN == 128 || BN == 256, "pair tile width");
+  static constexpr int kStageA = kBM * kBK;              // this CTA's 128 rows of A, one slab
+  static constexpr int kStageB = (BN / 2) * kBK;         // this CTA's half of the B tile
+  static constexpr int kStageBytes = kStageA + kStageB;
+  static constexpr int kStages = kPairRingBytes / kStageBytes;   // 6 or 8
+  static constexpr int kBufs = kTmemCols / BN;           // TMEM slab buffers: 2 or 4
+  static constexpr int kWarpCols = BN / 2;               // columns per promotion warp
+  static constexpr int kChunks = kWarpCols / 32;         // x32 TMEM loads per warp and slab
+};
 // Register split of the pair kernel: its producer warpgroup (TMA and MMA issue
 // loops) keeps 40 per thread so the promotion warpgroups can hold 232
 // (128 x 40 + 256 x 232 = 64512 = 168 x 384).
@@ -47,20 +62,22 @@ constexpr uint32_t kPairEpilogueRegs = 232;
 static_assert(128 * kPairProducerRegs + 256 * kPairEpilogueRegs <= 168 * kGemmThreads,
               "register split exceeds the launch budget");
 
+template <int BN>
 struct PairSmem {
   alignas(1024) unsigned char epi_stage[kEpiWarps][kEpiStageBytes];
-  uint64_t full[kPairStages];   // even CTA: both CTAs' loads of a slab have landed
-  uint64_t done[kPairStages];   // both CTAs: the slab's MMAs are complete
-  uint64_t tmem_free[2];        // even CTA: 16 promotion warps released a TMEM buffer
+  uint64_t full[PairCfg<BN>::kStages];   // even CTA: both CTAs' loads of a slab have landed
+  uint64_t done[PairCfg<BN>::kStages];   // both CTAs: the slab's MMAs are complete
+  uint64_t tmem_free[PairCfg<BN>::kBufs];  // even CTA: 16 promotion warps released a buffer
   uint64_t drain;
   uint32_t tmem_base;
   int32_t abort_flag;
   alignas(16) float sb_stage[kEpiWarps][2][128];
 };
 
-constexpr size_t kPairSmemBytes =
-    1024 /* alignment slack */ + static_cast<size_t>(kPairStages) * kPairStageBytes +
-    sizeof(PairSmem);
+template <int BN>
+constexpr size_t pair_smem_bytes() {
+  return 1024 /* alignment slack */ + static_cast<size_t>(kPairRingBytes) + sizeof(PairSmem<BN>);
+}
 
 // Work unit u of the persistent walk: a whole tile, or one K-range of a tail
 // tile (the tiles of the last, partial wave are split along K so that every
@@ -91,22 +108,22 @@ __device__ __forceinline__ PairUnit pair_unit(int u, const GemmParams& p) {
 // Sum of the K-range partials of the tail tiles, in split order, converted to
 // the output type (kAcc: added to the FP32 values already in C).  One thread
 // per 4 columns of one row of one tail tile.
-template <bool kOutBf16, bool kAcc = false>
+template <int BN, bool kOutBf16, bool kAcc = false>
 __global__ void __launch_bounds__(256) split_fixup_kernel(const float* __restrict__ ws,
                                                           GemmParams p, int tail_tiles) {
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int q = static_cast<int>(idx % 64);
-  const int r = static_cast<int>((idx / 64) % kPairTileM);
-  const int64_t tt = idx / (64 * kPairTileM);
+  const int q = static_cast<int>(idx % (BN / 4));
+  const int r = static_cast<int>((idx / (BN / 4)) % kPairTileM);
+  const int64_t tt = idx / ((BN / 4) * kPairTileM);
   if (tt >= tail_tiles) return;
   const int tile = p.full_tiles + static_cast<int>(tt);
   const int row = (tile % p.num_m_tiles) * kPairTileM + r;
-  const int col = (tile / p.num_m_tiles) * kBN + q * 4;
+  const int col = (tile / p.num_m_tiles) * BN + q * 4;
   if (row >= p.M || col >= p.N) return;   // N is a multiple of 16: col..col+3 < N
   float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int sp = 0; sp < p.splits; ++sp) {
     const float4 v = __ldcs(reinterpret_cast<const float4*>(
-        ws + ((tt * p.splits + sp) * kPairTileM + r) * static_cast<int64_t>(kBN) + q * 4));
+        ws + ((tt * p.splits + sp) * kPairTileM + r) * static_cast<int64_t>(BN) + q * 4));
     sum.x += v.x;
     sum.y += v.y;
     sum.z += v.z;
@@ -128,7 +145,7 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(const float* __restric
 
 // p.num_m_tiles counts 256-row pair tiles here.  kAcc (FP32 output only):
 // C += A * B^T, the tiles added into C by TMA reduce-add.
-template <int kSb, bool kOutBf16, bool kAcc = false>
+template <int BN, int kSb, bool kOutBf16, bool kAcc = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     fp8bs_gemm_pair_kernel(const __grid_constant__ GemmParams p,
                            const __grid_constant__ CUtensorMap tmap_a,
@@ -138,8 +155,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   extern __shared__ __align__(1024) unsigned char pair_smem_raw[];
   const uint32_t raw_addr = smem_u32(pair_smem_raw);
   unsigned char* ring = pair_smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  PairSmem& sm =
-      *reinterpret_cast<PairSmem*>(ring + static_cast<size_t>(kPairStages) * kPairStageBytes);
+  using Cfg = PairCfg<BN>;
+  PairSmem<BN>& sm = *reinterpret_cast<PairSmem<BN>*>(ring + static_cast<size_t>(kPairRingBytes));
   const uint32_t ring_addr = smem_u32(ring);
 
   const int warp = threadIdx.x >> 5;
@@ -152,11 +169,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPairStages; ++s) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.done[s], 1);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&sm.tmem_free[b], 2 * kEpiWarps);
+    for (int b = 0; b < Cfg::kBufs; ++b) mbar_init(&sm.tmem_free[b], 2 * kEpiWarps);
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbarrier_init();
@@ -187,20 +204,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       for (int u = PAIR_FIRST; u < p.units && !aborted; u += PAIR_STRIDE) {
         const PairUnit w = pair_unit(u, p);
         const int a_row = (w.tile % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM;
-        const int b_row = (w.tile / p.num_m_tiles) * kBN + static_cast<int>(rank) * (kBN / 2);
+        const int b_row = (w.tile / p.num_m_tiles) * BN + static_cast<int>(rank) * (BN / 2);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!bounded_wait(&sm.done[stage], phase ^ 1u, abort_flag)) {
             aborted = true;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(&sm.full[stage], 2 * kPairStageBytes);
+          if (rank == 0) mbar_arrive_expect_tx(&sm.full[stage], 2 * Cfg::kStageBytes);
           const uint32_t full_bar = mapa_shared(smem_u32(&sm.full[stage]), 0);
-          const uint32_t dst = ring_addr + stage * kPairStageBytes;
+          const uint32_t dst = ring_addr + stage * Cfg::kStageBytes;
           tma_load_2d_pair(dst, &tmap_a, kb * kBK, a_row, full_bar, policy_a);
-          tma_load_2d_pair(dst + kPairStageA, &tmap_b, kb * kBK, b_row, full_bar, policy_b);
+          tma_load_2d_pair(dst + Cfg::kStageA, &tmap_b, kb * kBK, b_row, full_bar, policy_b);
           issued_mask |= 1u << stage;
           parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
-          if (++stage == kPairStages) {
+          if (++stage == Cfg::kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -210,7 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // sees both CTAs' bytes on its `full` barriers; the odd CTA cannot wait
       // on them, so after an abort it gives its own copies time to land.
       if (rank == 0) {
-        for (int s = 0; s < kPairStages; ++s)
+        for (int s = 0; s < Cfg::kStages; ++s)
           if (issued_mask & (1u << s))
             bounded_wait_noabort(&sm.full[s], (parity_mask >> s) & 1u, kSpinLimitNs);
       } else if (aborted) {
@@ -218,7 +235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       }
     } else if (warp == 1 && lane == 0 && rank == 0) {
       // ---------------------------------------------------------------- MMA
-      constexpr uint32_t idesc = idesc_e4m3_f32(kPairTileM, kBN);
+      constexpr uint32_t idesc = idesc_e4m3_f32(kPairTileM, BN);
       int stage = 0, buf = 0;
       uint32_t phase = 0, tphase = 0;
       bool issued = false;
@@ -228,20 +245,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           if (!bounded_wait(&sm.full[stage], phase, abort_flag)) goto mma_done;
           if (!bounded_wait(&sm.tmem_free[buf], tphase ^ 1u, abort_flag)) goto mma_done;
           tc_fence_after();
-          const uint32_t a_addr = ring_addr + stage * kPairStageBytes;
+          const uint32_t a_addr = ring_addr + stage * Cfg::kStageBytes;
           const uint64_t adesc = smem_desc_k_sw128(a_addr);
-          const uint64_t bdesc = smem_desc_k_sw128(a_addr + kPairStageA);
-          const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
+          const uint64_t bdesc = smem_desc_k_sw128(a_addr + Cfg::kStageA);
+          const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
 #pragma unroll
           for (int kk = 0; kk < kBK / 32; ++kk)  // 32 bytes = 32 E4M3 values per MMA
             mma_f8f6f4_pair(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, kk > 0 ? 1u : 0u);
           mma_commit_pair(&sm.done[stage], 0x3);
           issued = true;
-          if (++stage == kPairStages) {
+          if (++stage == Cfg::kStages) {
             stage = 0;
             phase ^= 1u;
           }
-          if (++buf == 2) {
+          if (++buf == Cfg::kBufs) {
             buf = 0;
             tphase ^= 1u;
           }
@@ -257,7 +274,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     regs_alloc<kPairEpilogueRegs>();
     // ------------------------------------------------- promotion + epilogue
     const int g = warp & 3;          // TMEM lane group (rows 32g .. 32g+31 of this CTA)
-    const int h = (warp - 4) >> 2;   // column half (0: 0..127, 1: 128..255)
+    const int h = (warp - 4) >> 2;   // column half of the tile (kWarpCols columns each)
     int buf = 0, stage = 0;
     uint32_t phase = 0;
     for (int u = PAIR_FIRST; u < p.units; u += PAIR_STRIDE) {
@@ -265,11 +282,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const int t = w.tile;
       const int row = (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM + g * 32 + lane;
       const bool row_ok = row < p.M;
-      const int col0 = (t / p.num_m_tiles) * kBN + h * 128;
+      const int col0 = (t / p.num_m_tiles) * BN + h * Cfg::kWarpCols;
       const bool cols_ok = col0 < p.N;
-      float2 acc[64];
+      float2 acc[Cfg::kWarpCols / 2];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
+      for (int i = 0; i < Cfg::kWarpCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
       auto load_sa = [&](int kb) -> float {
         return (row_ok && kb < p.KB) ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ldsa + row)
@@ -306,7 +323,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         if (!bounded_wait(&sm.done[stage], phase, abort_flag)) goto epilogue_done;
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) +
-                               static_cast<uint32_t>(buf * kBN + h * 128);
+                               static_cast<uint32_t>(buf * BN + h * Cfg::kWarpCols);
         uint32_t ra[32], rb[32];
         tmem_ld32(taddr, ra);
         tmem_wait_ld(ra);
@@ -314,26 +331,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const float sc = sa_cur * sb_cur;
           const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-          for (int c = 0; c < 4; c += 2) {
+          for (int c = 0; c < Cfg::kChunks; c += 2) {
             tmem_ld32(taddr + (c + 1) * 32, rb);
             promote32(acc + c * 16, ra, sc2);
             tmem_wait_ld(rb);
-            if (c + 2 < 4) tmem_ld32(taddr + (c + 2) * 32, ra);
+            if (c + 2 < Cfg::kChunks) tmem_ld32(taddr + (c + 2) * 32, ra);
             promote32(acc + (c + 1) * 16, rb, sc2);
-            if (c + 2 < 4) tmem_wait_ld(ra);
+            if (c + 2 < Cfg::kChunks) tmem_wait_ld(ra);
           }
         } else {
           // columns past N carry zero scales (and zero products), so no guard is needed
           const float2 sa2 = make_float2(sa_cur, sa_cur);
           const float* sbs = sb_mine + (kb & 1) * 128;
 #pragma unroll
-          for (int c = 0; c < 4; c += 2) {
+          for (int c = 0; c < Cfg::kChunks; c += 2) {
             tmem_ld32(taddr + (c + 1) * 32, rb);
             promote32_percol(acc + c * 16, ra, sbs + c * 32, sa2);
             tmem_wait_ld(rb);
-            if (c + 2 < 4) tmem_ld32(taddr + (c + 2) * 32, ra);
+            if (c + 2 < Cfg::kChunks) tmem_ld32(taddr + (c + 2) * 32, ra);
             promote32_percol(acc + (c + 1) * 16, rb, sbs + (c + 1) * 32, sa2);
-            if (c + 2 < 4) tmem_wait_ld(ra);
+            if (c + 2 < Cfg::kChunks) tmem_wait_ld(ra);
           }
           reinterpret_cast<float4*>(sb_mine + ((kb + 1) & 1) * 128)[lane] = sbc_nxt;
           __syncwarp();
@@ -341,8 +358,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.tmem_free[buf]), 0));
-        buf ^= 1;
-        if (++stage == kPairStages) {
+        if (++buf == Cfg::kBufs) buf = 0;
+        if (++stage == Cfg::kStages) {
           stage = 0;
           phase ^= 1u;
         }
@@ -353,10 +370,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // (addresses are recomputed, not held: the promotion warps have no
       // registers to spare while the accumulators are live)
       if (w.slot < 0) {
-        store_rows_tma<kOutBf16, kAcc>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_c, col0,
+        store_rows_tma<kOutBf16, kAcc, Cfg::kWarpCols>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_c, col0,
                                  (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM + g * 32);
       } else {
-        store_rows_tma<false>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_ws, h * 128,
+        store_rows_tma<false, false, Cfg::kWarpCols>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_ws, h * Cfg::kWarpCols,
                               w.slot * kPairTileM + static_cast<int>(rank) * kBM + g * 32);
       }
     }
