@@ -410,6 +410,24 @@ def run_extras(dev, stream, peaks):
         "frac_fp8_peak_unpadded": round(flops_real / (med * 1e-3) / 1e12 / peaks["fp8_tflops"], 4)}
     del Aq, Bq, C, sa, sb
 
+    # quantize-then-dispatch of the same routing (16384 tokens x 7168, bf16)
+    expert = torch.from_numpy(wl.zipf_expert_ids().astype(np.int32)).to(dev)
+    T = int(expert.numel())
+    xt = torch.randn((T, K), device=dev, generator=gen).to(torch.bfloat16)
+    Mc = (T + 127 * E + 127) // 128 * 128
+    qd = torch.empty((Mc, K), dtype=torch.uint8, device=dev)
+    sd = torch.empty((K // 128, Mc), dtype=torch.float32, device=dev)
+    i32 = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
+    offd, cntd, t2r, r2t = i32(E + 1), i32(E), i32(T), i32(Mc)
+    md, _ = timeit(lambda: fb.fp8bs_quant_dispatch(xt, expert, E, qd, sd, offd, cntd, t2r, r2t,
+                                                   stream), flush=flush)
+    dbytes = quant_bytes(T * K, 2) + (M_cap - T) * (K + 4 * K / 128)   # + padding rows written
+    out["quant_dispatch_moe"] = {"tokens": T, "experts": E, "us": round(md * 1e3, 2),
+                                 "GB/s": round(dbytes / (md * 1e-3) / 1e9, 1),
+                                 "frac_hbm": round(dbytes / (md * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                 "launches": 4}
+    del xt, qd, sd
+
     # quantizer sweep
     sweep = {}
     for M in (1024, 8192, 65536):

@@ -27,6 +27,7 @@ FP8BS_ERR_UNSUPPORTED = 3
 FP8BS_ERR_CUDA = 4
 FP8BS_ERR_DEVICE_TIMEOUT = 5
 FP8BS_ERR_DEVICE_BAD_OFFSETS = 6
+FP8BS_ERR_DEVICE_BAD_ROUTING = 7
 FP8BS_F32 = 0
 FP8BS_BF16 = 1
 FP8BS_SB_BLOCK_NK = 0
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_quant_w_128x128.argtypes = [P, I, I64, I64, I64, P, I64, P, I64, P, I64, P]
         L.fp8bs_gemm_accumulate.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I, I64, P,
                                             I64, P, ctypes.c_size_t, P]
+        L.fp8bs_quant_dispatch.argtypes = [P, I, I64, I64, I64, P, I32, P, I64, P, I64, I64, P, P,
+                                           P, P, P]
         L.fp8bs_quant_act_dual.argtypes = [P, I, I64, I64, I64, P, I64, P, I64, P, I64, P, I64, P]
         L.fp8bs_gemm.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I, I64, P, I, I64, P]
         L.fp8bs_grouped_gemm.argtypes = [I32, P, I64, I64, I64, P, I64, P, I64, P, I64, P, I,
@@ -75,7 +78,7 @@ def lib() -> ctypes.CDLL:
                      "fp8bs_gemm", "fp8bs_grouped_gemm", "fp8bs_sync_status",
                      "fp8bs_debug_timeout_probe", "fp8bs_gemm_workspace_size", "fp8bs_gemm_ws",
                      "fp8bs_gemm_static_ws", "fp8bs_quant_act_dual", "fp8bs_gemm_accumulate",
-                     "fp8bs_probe_mma_f8f6f4"):
+                     "fp8bs_probe_mma_f8f6f4", "fp8bs_quant_dispatch"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -157,6 +160,19 @@ def fp8bs_quant_act_dual(x, q, s, qT, sT, stream=None):
                                       _row_stride(q), _ptr(s), _row_stride(s), _ptr(qT),
                                       _row_stride(qT), _ptr(sT), _row_stride(sT),
                                       _stream(stream)), "fp8bs_quant_act_dual")
+
+
+def fp8bs_quant_dispatch(x, expert, E: int, q, s, offsets, counts, token_row, row_token,
+                         stream=None):
+    """x [T x K] -> q [M_cap x K], s [K/128 x >=M_cap] in expert-grouped rows;
+    expert [T] int32 device; offsets [E+1], counts [E], token_row [T],
+    row_token [M_cap] int32 device outputs."""
+    T, K = x.shape
+    M_cap = q.shape[0]
+    _check(lib().fp8bs_quant_dispatch(_ptr(x), _dtype(x), T, K, _row_stride(x), _ptr(expert), E,
+                                      _ptr(q), _row_stride(q), _ptr(s), _row_stride(s), M_cap,
+                                      _ptr(offsets), _ptr(counts), _ptr(token_row),
+                                      _ptr(row_token), _stream(stream)), "fp8bs_quant_dispatch")
 
 
 def fp8bs_quant_w_128x128(w, q, qT, s, stream=None):

@@ -509,6 +509,51 @@ fp8bs_status fp8bs_quant_act_dual(const void* x, fp8bs_dtype xt, int64_t T, int6
   return launch_status();
 }
 
+fp8bs_status fp8bs_quant_dispatch(const void* x, fp8bs_dtype xt, int64_t T, int64_t K,
+                                  int64_t ldx, const int32_t* expert, int32_t E, uint8_t* q,
+                                  int64_t ldq, float* s, int64_t lds, int64_t M_cap,
+                                  int32_t* offsets, int32_t* counts, int32_t* token_row,
+                                  int32_t* row_token, void* stream) {
+  if (T < 0 || K < 0 || M_cap < 0 || !valid_dtype(xt)) return FP8BS_ERR_INVALID_ARG;
+  if (E < 1 || E > kDispatchMaxExperts) return FP8BS_ERR_UNSUPPORTED;
+  if (K % 128 != 0 || M_cap % 128 != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (M_cap < T + 127 * static_cast<int64_t>(E)) return FP8BS_ERR_INVALID_ARG;   // worst-case padding
+  if (T * (K / 128) > INT_MAX || M_cap > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+  if (offsets == nullptr || counts == nullptr || (T > 0 && (expert == nullptr || token_row == nullptr)))
+    return FP8BS_ERR_INVALID_ARG;
+  if (K > 0 && (x == nullptr || q == nullptr || s == nullptr || row_token == nullptr))
+    return FP8BS_ERR_INVALID_ARG;
+  if (K > 0 && (ldx < K || ldq < K || lds < M_cap)) return FP8BS_ERR_INVALID_ARG;
+  if (K > 0 && (!aligned(x, 16) || (ldx * static_cast<int64_t>(dtype_size(xt))) % 16 ||
+                !aligned(q, 16) || ldq % 16 || !aligned(s, 4)))
+    return FP8BS_ERR_MISALIGNED;
+  if (!aligned(offsets, 4) || !aligned(counts, 4)) return FP8BS_ERR_MISALIGNED;
+  cudaStream_t st = as_stream(stream);
+  DeviceInfo di;
+  fp8bs_status rc = device_info(&di);
+  if (rc != FP8BS_OK) return rc;
+  dispatch_plan_kernel<<<1, 1024, 0, st>>>(expert, T, E, token_row, counts, offsets);
+  if ((rc = launch_status()) != FP8BS_OK || T == 0 || K == 0) return rc;
+  const int64_t tiles = T * (K / 128);
+  int64_t blocks = (tiles + 63) / 64;
+  if (blocks > static_cast<int64_t>(di.num_sms) * 8) blocks = static_cast<int64_t>(di.num_sms) * 8;
+  if (xt == FP8BS_BF16)
+    quant_dispatch_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(T),
+        static_cast<uint32_t>(K / 128), ldx, expert, E, token_row, offsets, q, ldq, s, lds);
+  else
+    quant_dispatch_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const float*>(x), static_cast<uint32_t>(T), static_cast<uint32_t>(K / 128),
+        ldx, expert, E, token_row, offsets, q, ldq, s, lds);
+  if ((rc = launch_status()) != FP8BS_OK) return rc;
+  dispatch_rows_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, st>>>(
+      expert, T, E, offsets, token_row, row_token);
+  if ((rc = launch_status()) != FP8BS_OK) return rc;
+  dispatch_pad_kernel<<<static_cast<unsigned>(E), 256, 0, st>>>(
+      counts, offsets, static_cast<int>(K / 128), q, ldq, s, lds, row_token);
+  return launch_status();
+}
+
 fp8bs_status fp8bs_quant_w_128x128(const void* w, fp8bs_dtype wt, int64_t R, int64_t C,
                                    int64_t ldw, uint8_t* q, int64_t ldq, uint8_t* qT,
                                    int64_t ldqT, float* s, int64_t lds, void* stream) {
@@ -648,6 +693,7 @@ fp8bs_status fp8bs_sync_status(void* stream) {
     if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess)
       return FP8BS_ERR_CUDA;
     if (word & kDevErrTimeout) return FP8BS_ERR_DEVICE_TIMEOUT;
+    if (word & kDevErrBadRouting) return FP8BS_ERR_DEVICE_BAD_ROUTING;
     return FP8BS_ERR_DEVICE_BAD_OFFSETS;
   }
   return FP8BS_OK;
@@ -662,6 +708,7 @@ const char* fp8bs_status_string(fp8bs_status status) {
     case FP8BS_ERR_CUDA: return "CUDA error";
     case FP8BS_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case FP8BS_ERR_DEVICE_BAD_OFFSETS: return "grouped GEMM offsets failed device validation";
+    case FP8BS_ERR_DEVICE_BAD_ROUTING: return "expert id outside [0, E) in dispatch";
   }
   return "unknown status";
 }

@@ -12,7 +12,7 @@ namespace fp8bs {
 
 // Device error word (bit flags), read and cleared by fp8bs_sync_status().
 // The library is one translation unit (fp8bs.cu), so the definition lives here.
-enum : uint32_t { kDevErrTimeout = 1u, kDevErrBadOffsets = 2u };
+enum : uint32_t { kDevErrTimeout = 1u, kDevErrBadOffsets = 2u, kDevErrBadRouting = 4u };
 __device__ uint32_t g_device_error = 0;
 
 #ifndef FP8BS_SPIN_LIMIT_NS

@@ -498,4 +498,151 @@ __global__ void __launch_bounds__(256) quant_dual_kernel(const TIn* __restrict__
   }
 }
 
+// ------------------------------------------------ quantize-then-dispatch (MoE)
+// Activations quantized 1x128 straight into expert-grouped rows: expert e owns
+// rows offsets[e] .. offsets[e+1]-1 (its token count padded to a multiple of
+// 128), its tokens in increasing token order, then zero padding rows (codes 0,
+// scale 1: what quantizing a zero row gives).  Source: untitled page at
+// jp-study.kr, MoE passage (activations quantized to FP8 before the up-
+// projection and dispatched in FP8).
+constexpr int kDispatchMaxExperts = 256;
+
+// One CTA of 1024 threads: in chunks of 1024 tokens, each token's rank among
+// the earlier tokens of its expert (warp match + per-warp counts, prefix over
+// warps), then per-expert counts and padded offsets.  rank_out[t] = rank.
+__global__ void __launch_bounds__(1024) dispatch_plan_kernel(const int32_t* __restrict__ expert,
+                                                             int64_t T, int E,
+                                                             int32_t* __restrict__ rank_out,
+                                                             int32_t* __restrict__ counts,
+                                                             int32_t* __restrict__ offsets) {
+  __shared__ int32_t warp_cnt[32][kDispatchMaxExperts];
+  __shared__ int32_t running[kDispatchMaxExperts];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < kDispatchMaxExperts; e += 1024) running[e] = 0;
+  for (int64_t base = 0; base < T; base += 1024) {
+    for (int i = tid; i < 32 * kDispatchMaxExperts; i += 1024) (&warp_cnt[0][0])[i] = 0;
+    const int64_t t = base + tid;
+    int e = t < T ? expert[t] : -1;
+    if (t < T && (e < 0 || e >= E)) {   // routing outside [0, E): the token is dropped
+      atomicOr(&g_device_error, kDevErrBadRouting);
+      e = -1;
+    }
+    __syncthreads();
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    const int lane_rank = __popc(m & ((1u << lane) - 1u));
+    if (e >= 0 && lane_rank == 0) warp_cnt[warp][e] = __popc(m);
+    __syncthreads();
+    for (int x = tid; x < E; x += 1024) {   // exclusive prefix over the warps, per expert
+      int run = running[x];
+#pragma unroll 4
+      for (int w = 0; w < 32; ++w) {
+        const int c = warp_cnt[w][x];
+        warp_cnt[w][x] = run;
+        run += c;
+      }
+      running[x] = run;
+    }
+    __syncthreads();
+    if (e >= 0) rank_out[t] = warp_cnt[warp][e] + lane_rank;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    int32_t off = 0;
+    for (int e = 0; e < E; ++e) {
+      counts[e] = running[e];
+      offsets[e] = off;
+      off += (running[e] + 127) / 128 * 128;
+    }
+    offsets[E] = off;
+  }
+}
+
+// 1x128 quantization of token t's row into row offsets[e] + rank[t] (four lanes
+// per 128-element tile, as in quant_1x128_kernel).
+template <typename TIn>
+__global__ void __launch_bounds__(256) quant_dispatch_kernel(
+    const TIn* __restrict__ x, uint32_t T, uint32_t KB, int64_t ldx, const int32_t* __restrict__ expert,
+    int E, const int32_t* __restrict__ rank, const int32_t* __restrict__ offsets,
+    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s, int64_t lds) {
+  constexpr int kVec = Vec16<TIn>::kN;
+  constexpr int kLoads = 128 / (4 * kVec);
+  const int lane = threadIdx.x & 31;
+  const int sub = lane >> 2, l = lane & 3;
+  const uint32_t total = T * KB;
+  const uint32_t warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t num_warps = (gridDim.x * blockDim.x) >> 5;
+  for (uint32_t base = warp_id * 8; base < total; base += num_warps * 8) {
+    const uint32_t tile = base + sub;
+    const bool valid = tile < total;
+    const uint32_t t = valid ? tile / KB : 0, kb = valid ? tile - t * KB : 0;
+    const int e = valid ? expert[t] : -1;
+    const bool routed = valid && e >= 0 && e < E;
+    uint4 v[kLoads];
+    const TIn* src = x + static_cast<int64_t>(t) * ldx + kb * 128 + l * kVec;
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) v[i] = routed ? ld_stream16(src + i * 4 * kVec) : make_uint4(0, 0, 0, 0);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) {
+      float f[kVec];
+      Vec16<TIn>::widen(v[i], f);
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    float sc, r;
+    tile_scale(amax, sc, r);
+    if (routed) {
+      const int64_t row = static_cast<int64_t>(offsets[e]) + rank[t];
+      uint8_t* dst = q + row * ldq + kb * 128 + l * kVec;
+#pragma unroll
+      for (int i = 0; i < kLoads; ++i) {
+        float f[kVec];
+        Vec16<TIn>::widen(v[i], f);
+        if constexpr (kVec == 8) {
+          *reinterpret_cast<uint2*>(dst + i * 4 * kVec) = make_uint2(e4m3x4(f, r), e4m3x4(f + 4, r));
+        } else {
+          *reinterpret_cast<uint32_t*>(dst + i * 4 * kVec) = e4m3x4(f, r);
+        }
+      }
+      if (l == 0) s[static_cast<int64_t>(kb) * lds + row] = sc;
+    }
+  }
+}
+
+// token_row[t] = offsets[e] + rank[t] (rank read from token_row itself) and
+// row_token[row] = t.
+__global__ void dispatch_rows_kernel(const int32_t* __restrict__ expert, int64_t T, int E,
+                                     const int32_t* __restrict__ offsets,
+                                     int32_t* __restrict__ token_row,
+                                     int32_t* __restrict__ row_token) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const int e = expert[t];
+  if (e < 0 || e >= E) {
+    token_row[t] = -1;
+    return;
+  }
+  const int32_t row = offsets[e] + token_row[t];
+  token_row[t] = row;
+  row_token[row] = static_cast<int32_t>(t);
+}
+
+// Padding rows of expert blockIdx.x: codes 0, scales 1, row_token -1.
+__global__ void dispatch_pad_kernel(const int32_t* __restrict__ counts,
+                                    const int32_t* __restrict__ offsets, int KB,
+                                    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s,
+                                    int64_t lds, int32_t* __restrict__ row_token) {
+  const int e = blockIdx.x;
+  const int64_t r0 = static_cast<int64_t>(offsets[e]) + counts[e], r1 = offsets[e + 1];
+  const int64_t bytes_per_row = static_cast<int64_t>(KB) * 128;
+  for (int64_t r = r0; r < r1; ++r) {
+    uint4* dst = reinterpret_cast<uint4*>(q + r * ldq);
+    for (int64_t i = threadIdx.x; i < bytes_per_row / 16; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+    for (int kb = threadIdx.x; kb < KB; kb += blockDim.x) s[static_cast<int64_t>(kb) * lds + r] = 1.0f;
+    if (threadIdx.x == 0) row_token[r] = -1;
+  }
+}
+
 }  // namespace fp8bs

@@ -61,7 +61,8 @@ typedef enum fp8bs_status {
   FP8BS_ERR_UNSUPPORTED = 3,     /* shape outside the supported set (e.g. K % 128) */
   FP8BS_ERR_CUDA = 4,            /* CUDA runtime / launch error */
   FP8BS_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up on a device-side wait */
-  FP8BS_ERR_DEVICE_BAD_OFFSETS = 6 /* grouped GEMM offsets failed device validation */
+  FP8BS_ERR_DEVICE_BAD_OFFSETS = 6, /* grouped GEMM offsets failed device validation */
+  FP8BS_ERR_DEVICE_BAD_ROUTING = 7  /* dispatch: an expert id outside [0, E) */
 } fp8bs_status;
 
 typedef enum fp8bs_dtype { FP8BS_F32 = 0, FP8BS_BF16 = 1 } fp8bs_dtype;
@@ -119,6 +120,35 @@ fp8bs_status fp8bs_quant_act_dual(const void* x, fp8bs_dtype xt, int64_t T, int6
                                   int64_t ldx, uint8_t* q, int64_t ldq, float* s, int64_t lds,
                                   uint8_t* qT, int64_t ldqT, float* sT, int64_t ldsT,
                                   void* stream);
+
+/* Quantize-then-dispatch for MoE layers: activations quantized 1x128 directly
+ * into expert-grouped rows, the A operand of fp8bs_grouped_gemm (untitled page
+ * at jp-study.kr, MoE passage: activations are quantized to FP8 before the
+ * up-projection and dispatched in FP8).
+ *   x       [T x K] fp32 or bf16 (row stride ldx), one row per token;
+ *   expert  [T] device int32, the expert of each token, in [0, E);
+ *   outputs (device, caller-owned):
+ *     offsets   [E+1]: expert e owns rows offsets[e] .. offsets[e+1]-1; its
+ *               token count is padded to a multiple of 128;
+ *     counts    [E]: tokens per expert (before padding);
+ *     q, s      rows as fp8bs_quant_act_1x128 would write for the rows
+ *               x[token] (q [M_cap x K], ldq; s[kb*lds + row], lds >= M_cap);
+ *               within an expert, tokens in increasing token order; padding
+ *               rows get codes 0 and scale 1 (a quantized zero row);
+ *     token_row [T]: the row of each token;  row_token [M_cap]: the token of
+ *               each row, -1 on padding rows.
+ *   Rows at or past offsets[E] are left untouched.
+ * Requirements: 1 <= E <= 256 and K % 128 == 0 and M_cap % 128 == 0
+ * (UNSUPPORTED); M_cap >= T + 127 * E, the worst-case padded size
+ * (INVALID_ARG); x, q 16-byte aligned, ldx*sizeof(xt) and ldq multiples of 16
+ * (MISALIGNED).  An expert id outside [0, E) drops that token and is reported
+ * by fp8bs_sync_status as FP8BS_ERR_DEVICE_BAD_ROUTING.  Four launches on the
+ * stream (plan, quantize, row maps, padding). */
+fp8bs_status fp8bs_quant_dispatch(const void* x, fp8bs_dtype xt, int64_t T, int64_t K,
+                                  int64_t ldx, const int32_t* expert, int32_t E, uint8_t* q,
+                                  int64_t ldq, float* s, int64_t lds, int64_t M_cap,
+                                  int32_t* offsets, int32_t* counts, int32_t* token_row,
+                                  int32_t* row_token, void* stream);
 
 /* 128x128 weight quantizer (one scale per 128 x 128 block).
  *   w  [R x C] fp32 or bf16, row stride ldw >= C.
@@ -236,8 +266,9 @@ fp8bs_status fp8bs_grouped_gemm(int32_t E, const int32_t* offsets, int64_t M_cap
                                 void* C, fp8bs_dtype ct, int64_t ldc, void* stream);
 
 /* Synchronize the stream, then report (and clear) the device error word of the
- * current device: FP8BS_ERR_DEVICE_TIMEOUT, FP8BS_ERR_DEVICE_BAD_OFFSETS,
- * FP8BS_ERR_CUDA for a sticky CUDA error, else FP8BS_OK. */
+ * current device: FP8BS_ERR_DEVICE_TIMEOUT, FP8BS_ERR_DEVICE_BAD_ROUTING,
+ * FP8BS_ERR_DEVICE_BAD_OFFSETS (in that order of precedence), FP8BS_ERR_CUDA
+ * for a sticky CUDA error, else FP8BS_OK. */
 fp8bs_status fp8bs_sync_status(void* stream);
 
 /* Static string naming a status code. */

@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for st in range(7):
+    for st in range(8):
         assert fb.status_string(st) not in ("", "unknown status")
     assert fb.status_string(99) == "unknown status"
 
@@ -137,3 +137,13 @@ def test_gemm_ws_host_checks(L):
                            None) == fb.FP8BS_ERR_UNSUPPORTED
     assert L.fp8bs_gemm_ws(0, 256, 128, NULL, 128, NULL, 128, NULL, 128, NULL,
                            fb.FP8BS_SB_BLOCK_KN, 2, NULL, BF16, 256, NULL, 0, None) == fb.FP8BS_OK
+
+
+def test_dispatch_host_checks(L):
+    args = lambda E, M_cap, K=128, T=100: (FAKE, BF16, T, K, K, FAKE, E, FAKE, K, FAKE, M_cap,  # noqa: E731
+                                          M_cap, FAKE, FAKE, FAKE, FAKE, None)
+    assert L.fp8bs_quant_dispatch(*args(0, 1024)) == fb.FP8BS_ERR_UNSUPPORTED       # E < 1
+    assert L.fp8bs_quant_dispatch(*args(257, 40960)) == fb.FP8BS_ERR_UNSUPPORTED    # E > 256
+    assert L.fp8bs_quant_dispatch(*args(4, 1024, K=100)) == fb.FP8BS_ERR_UNSUPPORTED
+    assert L.fp8bs_quant_dispatch(*args(4, 512)) == fb.FP8BS_ERR_INVALID_ARG         # < T + 127 E
+    assert L.fp8bs_quant_dispatch(*args(4, 1000)) == fb.FP8BS_ERR_UNSUPPORTED        # M_cap % 128

@@ -85,12 +85,19 @@ def layer_grad_output(tokens: int = TOKENS, n_out: int = FFN, seed: int = 2) -> 
     return to_bf16(rng.standard_normal((tokens, n_out), dtype=np.float32) * np.float32(1e-3))
 
 
-def zipf_counts(experts: int = EXPERTS, rows: int = ROUTED_ROWS, s: float = ZIPF_S,
-                seed: int = 3) -> np.ndarray:
+def zipf_expert_ids(experts: int = EXPERTS, rows: int = ROUTED_ROWS, s: float = ZIPF_S,
+                    seed: int = 3) -> np.ndarray:
+    """Expert of each routed token: a categorical over ranks 1..experts with
+    p ~ rank^-s, seeded."""
     rng = np.random.default_rng(seed)
     p = (np.arange(1, experts + 1, dtype=np.float64)) ** (-s)
     p /= p.sum()
-    choice = rng.choice(experts, size=rows, p=p)
+    return rng.choice(experts, size=rows, p=p).astype(np.int64)
+
+
+def zipf_counts(experts: int = EXPERTS, rows: int = ROUTED_ROWS, s: float = ZIPF_S,
+                seed: int = 3) -> np.ndarray:
+    choice = zipf_expert_ids(experts, rows, s, seed)
     return np.bincount(choice, minlength=experts).astype(np.int64)
 
 
