@@ -57,9 +57,10 @@ def dual_bytes(elems: int, in_bytes: int) -> float:
 # DRAM traffic per launch measured by ncu (dram__bytes_read.sum + write.sum), with
 # the sha256 of the kernel source it was measured on; ignored once the source changes.
 NCU_TRAFFIC = {
-    # ncu --set full, one launch of `bench.py --case wgrad` (profiles/gemm_pair_layer_ncu_full.md)
-    "gemm_wgrad": {"file": "gemm_pair_kernel.cuh", "src": "a5472a50fd78df0d",
-                   "bytes": 192056064 + 496465664},
+    # ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch of
+    # `bench.py --case wgrad` (profiles/gemm_pair_layer_ncu_full.md)
+    "gemm_wgrad": {"file": "gemm_pair_kernel.cuh", "src": "5a84dda834249ad8",
+                   "bytes": 198185728 + 495815424},
 }
 
 
