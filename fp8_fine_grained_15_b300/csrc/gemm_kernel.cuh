@@ -75,6 +75,7 @@ struct GemmParams {
   int32_t full_tiles;
   int32_t splits;
   int32_t units;
+  int32_t group_m;   // pair kernel: m tiles per group of the tile walk (>= 1)
 };
 
 struct GemmSmem {

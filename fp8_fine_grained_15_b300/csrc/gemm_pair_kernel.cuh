@@ -79,6 +79,20 @@ constexpr size_t pair_smem_bytes() {
   return 1024 /* alignment slack */ + static_cast<size_t>(kPairRingBytes) + sizeof(PairSmem<BN>);
 }
 
+// Output tile t of the walk -> (m tile, n tile): groups of p.group_m m tiles,
+// within a group m fastest, then n.  A wave of clusters then covers about
+// group_m x (clusters / group_m) tiles, so both its A and its B panels stay in
+// L2 (with all m tiles in one group, the wave's A panels are all of A and are
+// re-read from DRAM every wave when A and a wave's B exceed L2).
+__device__ __forceinline__ void pair_tile_mn(int t, const GemmParams& p, int& mt, int& nt) {
+  const int per_group = p.group_m * p.num_n_tiles;
+  const int first = (t / per_group) * p.group_m;
+  const int rows = p.num_m_tiles - first < p.group_m ? p.num_m_tiles - first : p.group_m;
+  const int l = t - (t / per_group) * per_group;
+  mt = first + l % rows;
+  nt = l / rows;
+}
+
 // Work unit u of the persistent walk: a whole tile, or one K-range of a tail
 // tile (the tiles of the last, partial wave are split along K so that every
 // cluster has work; their FP32 partials are summed by split_fixup_kernel).
@@ -117,8 +131,10 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(const float* __restric
   const int64_t tt = idx / ((BN / 4) * kPairTileM);
   if (tt >= tail_tiles) return;
   const int tile = p.full_tiles + static_cast<int>(tt);
-  const int row = (tile % p.num_m_tiles) * kPairTileM + r;
-  const int col = (tile / p.num_m_tiles) * BN + q * 4;
+  int mt, nt;
+  pair_tile_mn(tile, p, mt, nt);
+  const int row = mt * kPairTileM + r;
+  const int col = nt * BN + q * 4;
   if (row >= p.M || col >= p.N) return;   // N is a multiple of 16: col..col+3 < N
   float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int sp = 0; sp < p.splits; ++sp) {
@@ -203,8 +219,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       bool aborted = false;
       for (int u = PAIR_FIRST; u < p.units && !aborted; u += PAIR_STRIDE) {
         const PairUnit w = pair_unit(u, p);
-        const int a_row = (w.tile % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM;
-        const int b_row = (w.tile / p.num_m_tiles) * BN + static_cast<int>(rank) * (BN / 2);
+        int mt, nt;
+        pair_tile_mn(w.tile, p, mt, nt);
+        const int a_row = mt * kPairTileM + static_cast<int>(rank) * kBM;
+        const int b_row = nt * BN + static_cast<int>(rank) * (BN / 2);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!bounded_wait(&sm.done[stage], phase ^ 1u, abort_flag)) {
             aborted = true;
@@ -279,10 +297,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     for (int u = PAIR_FIRST; u < p.units; u += PAIR_STRIDE) {
       const PairUnit w = pair_unit(u, p);
-      const int t = w.tile;
-      const int row = (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM + g * 32 + lane;
+      int mt, nt;
+      pair_tile_mn(w.tile, p, mt, nt);
+      const int row = mt * kPairTileM + static_cast<int>(rank) * kBM + g * 32 + lane;
       const bool row_ok = row < p.M;
-      const int col0 = (t / p.num_m_tiles) * BN + h * Cfg::kWarpCols;
+      const int col0 = nt * BN + h * Cfg::kWarpCols;
       const bool cols_ok = col0 < p.N;
       float2 acc[Cfg::kWarpCols / 2];
 #pragma unroll
@@ -292,12 +311,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         return (row_ok && kb < p.KB) ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ldsa + row)
                                      : 0.0f;
       };
+      // block mode: this warp's column block of B scales (one pointer kept)
+      const float* sb_blk = p.sb + static_cast<int64_t>(col0 / 128) * p.sb_n_stride;
       auto load_sb = [&](int kb) -> float {
         if constexpr (kSb == kSbBlock) {
-          return (cols_ok && kb < p.KB)
-                     ? __ldg(p.sb + static_cast<int64_t>(kb) * p.sb_k_stride +
-                             static_cast<int64_t>(col0 / 128) * p.sb_n_stride)
-                     : 0.0f;
+          return (cols_ok && kb < p.KB) ? __ldg(sb_blk + static_cast<int64_t>(kb) * p.sb_k_stride)
+                                        : 0.0f;
         } else {
           return 0.0f;
         }
@@ -371,7 +390,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // registers to spare while the accumulators are live)
       if (w.slot < 0) {
         store_rows_tma<kOutBf16, kAcc, Cfg::kWarpCols>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_c, col0,
-                                 (t % p.num_m_tiles) * kPairTileM + static_cast<int>(rank) * kBM + g * 32);
+                                 row - lane);
       } else {
         store_rows_tma<false, false, Cfg::kWarpCols>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_ws, h * Cfg::kWarpCols,
                               w.slot * kPairTileM + static_cast<int>(rank) * kBM + g * 32);
