@@ -59,8 +59,8 @@ def dual_bytes(elems: int, in_bytes: int) -> float:
 NCU_TRAFFIC = {
     # ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch of
     # `bench.py --case wgrad` (profiles/gemm_pair_layer_ncu_full.md)
-    "gemm_wgrad": {"file": "gemm_pair_kernel.cuh", "src": "5a84dda834249ad8",
-                   "bytes": 198185728 + 495815424},
+    "gemm_wgrad": {"file": "gemm_pair_kernel.cuh", "src": "04c1dbfdadbd7d84",
+                   "bytes": 191641344 + 496067328},
 }
 
 
