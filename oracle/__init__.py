@@ -7,6 +7,8 @@ package and this package never imports the product library.
 The arithmetic lives in ``fp8bs_oracle.c`` (plain C, binary32 quantization,
 binary64 GEMM); this module compiles it with gcc on first use and wraps it with
 numpy arrays.  Grouped GEMM is the dense oracle applied expert by expert.
+The MX variant (UE8M0 power-of-two scales on 1x32 groups, applied per group)
+has its own quantizer and GEMM in the same file.
 
 Every function cites the passage it restates in the C source's header.  Pins
 (tests/test_oracle_pins.py) tie it to the OCP E4M3 format, to PyTorch's own
@@ -58,8 +60,13 @@ def _load():
         lib.fp8bs_oracle_gemm.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I, I64, P, P]
         lib.fp8bs_oracle_gemm_elements.argtypes = [I64, P, I64, P, I64, P, I64, P, I, I64,
                                                    I64, P, P, P, P]
+        lib.fp8bs_oracle_mx_quant_1x32.argtypes = [P, I, I64, I64, I64, P, I64, P, I64]
+        lib.fp8bs_oracle_mx_gemm.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I64,
+                                             P, P]
+        lib.fp8bs_oracle_mx_gemm_elements.argtypes = [I64, P, I64, P, I64, P, I64, P, I64,
+                                                      I64, P, P, P, P]
         for f in ("quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm",
-                  "gemm_elements"):
+                  "gemm_elements", "mx_quant_1x32", "mx_gemm", "mx_gemm_elements"):
             getattr(lib, "fp8bs_oracle_" + f).restype = None
         _lib = lib
     return _lib
@@ -225,4 +232,65 @@ def grouped_gemm_elements(offsets, A, sa, B, sb, sb_mode: int, rows, cols):
         ce, ae = gemm_elements(A[r0:r1], sa[:, r0:r1], B[e], sb[e], sb_mode,
                                rows[sel] - r0, cols[sel])
         c[sel], a[sel] = ce, ae
+    return c, a
+
+
+# ------------------------------------------------------------ MX variant
+
+def mx_quant_1x32(x: np.ndarray):
+    """1x32 groups along K with power-of-two (UE8M0) scales.  x [R x K]
+    (float32 or bf16 bits) -> (q [R x K] uint8, sf [K/128 x R x 4] uint8):
+    sf[kb, r, j] = e + 127 for the group of columns 128*kb + 32*j .. +31 of
+    row r, whose values were multiplied by 2^-e before the E4M3 rounding."""
+    x, dt = _as_input(x)
+    R, K = x.shape
+    assert K % 128 == 0
+    q = np.zeros((R, K), np.uint8)
+    sf = np.zeros((K // 128, R, 4), np.uint8)
+    _load().fp8bs_oracle_mx_quant_1x32(_ptr(x), dt, R, K, K, _ptr(q), K, _ptr(sf), R)
+    return q, sf
+
+
+def mx_dequant(q: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    """dec(q[r][k]) * 2^(sf byte of (r, k/32) - 127), fp64."""
+    dec = e4m3_decode_table()
+    R, K = q.shape
+    e = sf.transpose(1, 0, 2).reshape(R, K // 32).astype(np.int64) - 127
+    return dec[q] * np.ldexp(1.0, np.repeat(e, 32, axis=1))
+
+
+def mx_gemm(A: np.ndarray, sfa: np.ndarray, B: np.ndarray, sfb: np.ndarray):
+    """MX GEMM by definition: C = A * B^T with each 32-deep group's product sum
+    multiplied by 2^(ea + eb).  A [M x K], B [N x K] codes; sfa [K/128 x M x 4],
+    sfb [K/128 x N x 4].  Returns (C_ref, S_abs), float64 [M x N]."""
+    A = np.ascontiguousarray(A, np.uint8)
+    B = np.ascontiguousarray(B, np.uint8)
+    sfa = np.ascontiguousarray(sfa, np.uint8)
+    sfb = np.ascontiguousarray(sfb, np.uint8)
+    M, K = A.shape
+    N = B.shape[0]
+    assert B.shape[1] == K and K % 128 == 0
+    assert sfa.shape == (K // 128, M, 4) and sfb.shape == (K // 128, N, 4)
+    c = np.zeros((M, N), np.float64)
+    a = np.zeros((M, N), np.float64)
+    _load().fp8bs_oracle_mx_gemm(M, N, K, _ptr(A), K, _ptr(sfa), M, _ptr(B), K, _ptr(sfb), N,
+                                 _ptr(c), _ptr(a))
+    return c, a
+
+
+def mx_gemm_elements(A, sfa, B, sfb, rows, cols):
+    """mx_gemm() at the listed (row, col) positions only."""
+    A = np.ascontiguousarray(A, np.uint8)
+    B = np.ascontiguousarray(B, np.uint8)
+    sfa = np.ascontiguousarray(sfa, np.uint8)
+    sfb = np.ascontiguousarray(sfb, np.uint8)
+    rows = np.ascontiguousarray(rows, np.int64)
+    cols = np.ascontiguousarray(cols, np.int64)
+    M, K = A.shape
+    N = B.shape[0]
+    assert sfa.shape == (K // 128, M, 4) and sfb.shape == (K // 128, N, 4)
+    c = np.zeros(rows.size, np.float64)
+    a = np.zeros(rows.size, np.float64)
+    _load().fp8bs_oracle_mx_gemm_elements(K, _ptr(A), K, _ptr(sfa), M, _ptr(B), K, _ptr(sfb), N,
+                                          rows.size, _ptr(rows), _ptr(cols), _ptr(c), _ptr(a))
     return c, a

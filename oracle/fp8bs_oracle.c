@@ -298,3 +298,121 @@ void fp8bs_oracle_gemm_elements(int64_t K,
         gemm_one(K, A, lda, sa, ldsa, B, ldb, sb, mode, ldsb, dec, rows[e], cols[e],
                  &c_ref[e], &s_abs[e]);
 }
+
+/* ------------------------------------------------- MX (microscaling) variant
+ *
+ * Sources: "Should Fixing Deepseek Take 60 Steps?", Figure 7 (a) passage and
+ * the page at why-be.why-be.co.kr, accumulation-precision passage: both point
+ * to microscaling formats, with group scaling done by the tensor cores of the
+ * next GPU generation, as the direction fine-grained quantization takes.
+ *
+ * Readings taken where the pages are silent (each is listed in the design doc):
+ *  - Groups are 1x32 along the contraction axis for both operands.  A group's
+ *    scale is a power of two 2^e stored as an unsigned 8-bit exponent
+ *    (UE8M0: byte = e + 127, e in [-127, 127]).
+ *  - e is the smallest integer with amax <= 448 * 2^e (the scale rounded up to
+ *    a power of two, so no element overflows), clamped to [-127, 127]; an
+ *    all-zero group gets e = 0.
+ *  - code = enc(fl32(x * 2^-e)): one binary32 multiply by an exact power of
+ *    two, then the E4M3 rounding of the tile quantizers.
+ *  - Storage of the exponent bytes: the four groups of one row inside one
+ *    128-wide K block share a 32-bit word, group 4kb+j in byte j:
+ *    sf[(kb*ldsf + r)*4 + j], ldsf >= rows.
+ */
+
+/* Smallest e with amax <= 448 * 2^e, searched from a log2 estimate. */
+static int mx_group_exponent(float amax)
+{
+    int e;
+    if (amax == 0.0f)
+        return 0;
+    e = (int)ceil(log2((double)amax / 448.0));
+    while ((double)amax > ldexp(448.0, e))
+        ++e;
+    while ((double)amax <= ldexp(448.0, e - 1))
+        --e;
+    if (e < -127)
+        e = -127;
+    if (e > 127)
+        e = 127;
+    return e;
+}
+
+/* x [R x K] row-major (ldx elements) -> q [R x K] (ldq bytes per row) and the
+ * exponent bytes sf as described above.  K % 128 == 0. */
+void fp8bs_oracle_mx_quant_1x32(const void *x, int dtype, int64_t R, int64_t K, int64_t ldx,
+                                uint8_t *q, int64_t ldq, uint8_t *sf, int64_t ldsf)
+{
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t g = 0; g < K / 32; ++g) {
+            float amax = 0.0f, mult;
+            int e;
+            for (int c = 0; c < 32; ++c) {
+                float a = fabsf(load_elem(x, dtype, ldx, r, g * 32 + c));
+                if (a > amax)
+                    amax = a;
+            }
+            e = mx_group_exponent(amax);
+            mult = ldexpf(1.0f, -e);       /* exact: 2^-127 .. 2^127 are binary32 values */
+            for (int c = 0; c < 32; ++c) {
+                volatile float y = load_elem(x, dtype, ldx, r, g * 32 + c) * mult;
+                q[r * ldq + g * 32 + c] = fp8bs_oracle_e4m3_encode(y);
+            }
+            sf[((g / 4) * ldsf + r) * 4 + g % 4] = (uint8_t)(e + 127);
+        }
+    }
+}
+
+/* One output element of the MX GEMM
+ *   C[i][j] = sum over 32-deep K groups g of
+ *             ( sum_{k in g} dec(A[i][k]) * dec(B[j][k]) ) * 2^(ea(i,g) + eb(j,g))
+ * A [M x K] codes (lda), B [N x K] codes (ldb); exponent bytes as above.
+ * Also S_abs = sum_k |a_ik * b_jk| over the dequantized operands. */
+static void mx_gemm_one(int64_t K, const uint8_t *A, int64_t lda, const uint8_t *sfa,
+                        int64_t ldsfa, const uint8_t *B, int64_t ldb, const uint8_t *sfb,
+                        int64_t ldsfb, const double *dec, int64_t i, int64_t j,
+                        double *c_out, double *abs_out)
+{
+    double c = 0.0, sabs = 0.0;
+    for (int64_t g = 0; g < K / 32; ++g) {
+        double part = 0.0, part_abs = 0.0, scale;
+        int ea = (int)sfa[((g / 4) * ldsfa + i) * 4 + g % 4] - 127;
+        int eb = (int)sfb[((g / 4) * ldsfb + j) * 4 + g % 4] - 127;
+        scale = ldexp(1.0, ea + eb);
+        for (int64_t k = g * 32; k < g * 32 + 32; ++k) {
+            double p = dec[A[i * lda + k]] * dec[B[j * ldb + k]];
+            part += p;
+            part_abs += fabs(p);
+        }
+        c += part * scale;
+        sabs += part_abs * scale;
+    }
+    *c_out = c;
+    *abs_out = sabs;
+}
+
+void fp8bs_oracle_mx_gemm(int64_t M, int64_t N, int64_t K,
+                          const uint8_t *A, int64_t lda, const uint8_t *sfa, int64_t ldsfa,
+                          const uint8_t *B, int64_t ldb, const uint8_t *sfb, int64_t ldsfb,
+                          double *c_ref, double *s_abs)
+{
+    double dec[256];
+    decode_table(dec);
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j)
+            mx_gemm_one(K, A, lda, sfa, ldsfa, B, ldb, sfb, ldsfb, dec, i, j,
+                        &c_ref[i * N + j], &s_abs[i * N + j]);
+}
+
+void fp8bs_oracle_mx_gemm_elements(int64_t K,
+                                   const uint8_t *A, int64_t lda, const uint8_t *sfa, int64_t ldsfa,
+                                   const uint8_t *B, int64_t ldb, const uint8_t *sfb, int64_t ldsfb,
+                                   int64_t count, const int64_t *rows, const int64_t *cols,
+                                   double *c_ref, double *s_abs)
+{
+    double dec[256];
+    decode_table(dec);
+    for (int64_t e = 0; e < count; ++e)
+        mx_gemm_one(K, A, lda, sfa, ldsfa, B, ldb, sfb, ldsfb, dec, rows[e], cols[e],
+                    &c_ref[e], &s_abs[e]);
+}
