@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
                                     ctypes.c_size_t, P]
         L.fp8bs_gemm_static_ws.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I, I64, P, I,
                                            I64, P]
+        L.fp8bs_mx_quant_1x32.argtypes = [P, I, I64, I64, I64, P, I64, P, I64, P]
+        L.fp8bs_mx_gemm.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, I64, P, I, I64, P]
         L.fp8bs_sync_status.argtypes = [P]
         L.fp8bs_status_string.argtypes = [I]
         L.fp8bs_status_string.restype = ctypes.c_char_p
@@ -78,7 +80,8 @@ def lib() -> ctypes.CDLL:
                      "fp8bs_gemm", "fp8bs_grouped_gemm", "fp8bs_sync_status",
                      "fp8bs_debug_timeout_probe", "fp8bs_gemm_workspace_size", "fp8bs_gemm_ws",
                      "fp8bs_gemm_static_ws", "fp8bs_quant_act_dual", "fp8bs_gemm_accumulate",
-                     "fp8bs_probe_mma_f8f6f4", "fp8bs_quant_dispatch"):
+                     "fp8bs_probe_mma_f8f6f4", "fp8bs_quant_dispatch", "fp8bs_mx_quant_1x32",
+                     "fp8bs_mx_gemm"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -252,6 +255,34 @@ def fp8bs_grouped_gemm(offsets, A, sa, B, sb, sb_mode: int, C, stream=None):
                                     _ptr(sa), _row_stride(sa), _ptr(B), B.stride(1), _ptr(sb),
                                     sb_mode, sb.stride(1), sb.stride(0), _ptr(C), _dtype(C),
                                     _row_stride(C), _stream(stream)), "fp8bs_grouped_gemm")
+
+
+def _words(sf):
+    """Row stride, in 32-bit words, of an exponent-word tensor: int32 [K/128 x ld]."""
+    import torch
+    if sf.dtype != torch.int32 or sf.dim() != 2 or sf.stride(1) != 1:
+        raise ValueError("MX exponent words must be a 2-D int32 tensor with unit column stride")
+    return sf.stride(0)
+
+
+def fp8bs_mx_quant_1x32(x, q, sf, stream=None):
+    """x [R x K] bf16/fp32 -> q [R x K] uint8 codes and sf [K/128 x ld>=R] int32
+    words of four UE8M0 group exponents (group 4kb+j in byte j)."""
+    R, K = x.shape
+    _check(lib().fp8bs_mx_quant_1x32(_ptr(x), _dtype(x), R, K, _row_stride(x), _ptr(q),
+                                     _row_stride(q), _ptr(sf), _words(sf), _stream(stream)),
+           "fp8bs_mx_quant_1x32")
+
+
+def fp8bs_mx_gemm(A, sfa, B, sfb, C, stream=None):
+    """C [M x N] (bf16/fp32) = A [M x K] * B [N x K]^T with the MX group
+    exponents sfa [K/128 x >=M], sfb [K/128 x >=N] (int32 words)."""
+    M, K = A.shape
+    N = B.shape[0]
+    _check(lib().fp8bs_mx_gemm(M, N, K, _ptr(A), _row_stride(A), _ptr(sfa), _words(sfa), _ptr(B),
+                               _row_stride(B), _ptr(sfb), _words(sfb), _ptr(C), _dtype(C),
+                               _row_stride(C), _stream(stream)),
+           "fp8bs_mx_gemm")
 
 
 def fp8bs_sync_status(stream=None) -> int:

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libfp8bs.so")
 SOURCES = [os.path.join(CSRC, "fp8bs.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "quant_kernels.cuh", "gemm_pair_kernel.cuh",
-                                                  "gemm_kernel.cuh")] + \
+                                                  "gemm_mx_kernel.cuh", "gemm_kernel.cuh")] + \
     [os.path.join(ROOT, "include", "fp8bs.h")]
 
 NVCC_FLAGS = [

@@ -12,6 +12,7 @@
 
 #include "../../include/fp8bs.h"
 #include "gemm_kernel.cuh"
+#include "gemm_mx_kernel.cuh"
 #include "gemm_pair_kernel.cuh"
 #include "quant_kernels.cuh"
 
@@ -173,6 +174,23 @@ fp8bs_status make_map_out(CUtensorMap* m, void* base, fp8bs_dtype ct, uint64_t c
                    2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
+// Map over the MX exponent words [KB][ld_words] (uint32, `rows` used per K
+// block), box = box_rows words x 1 K block, no swizzle.
+fp8bs_status make_map_sf(CUtensorMap* m, const void* base, uint64_t rows, uint64_t KB,
+                         uint64_t ld_words, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  fp8bs_status st = encode_fn(&enc);
+  if (st != FP8BS_OK) return st;
+  cuuint64_t dims[2] = {rows, KB};
+  cuuint64_t strides[1] = {ld_words * 4};
+  cuuint32_t box[2] = {box_rows, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
 }
 
@@ -732,6 +750,75 @@ fp8bs_status fp8bs_probe_mma_f8f6f4(const uint8_t* a, const uint8_t* b, int64_t 
   fp8bs_mma_probe_kernel<<<1, 128, kProbeSmemBytes, as_stream(stream)>>>(a, b, static_cast<int>(K),
                                                                          d);
   return launch_status();
+}
+
+fp8bs_status fp8bs_mx_quant_1x32(const void* x, fp8bs_dtype xt, int64_t R, int64_t K, int64_t ldx,
+                                 uint8_t* q, int64_t ldq, uint32_t* sf, int64_t ldsf,
+                                 void* stream) {
+  if (R < 0 || K < 0 || !valid_dtype(xt)) return FP8BS_ERR_INVALID_ARG;
+  if (K % 128 != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (R == 0 || K == 0) return FP8BS_OK;
+  if ((R + 7) / 8 > INT_MAX || (K + 1023) / 1024 > 65535) return FP8BS_ERR_UNSUPPORTED;
+  if (x == nullptr || q == nullptr || sf == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (ldx < K || ldq < K || ldsf < R) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(q, 16) || (ldx * static_cast<int64_t>(dtype_size(xt))) % 16 ||
+      ldq % 16 || !aligned(sf, 4))
+    return FP8BS_ERR_MISALIGNED;
+  const dim3 grid(static_cast<unsigned>((R + 7) / 8), static_cast<unsigned>((K + 1023) / 1024));
+  if (xt == FP8BS_BF16)
+    mx_quant_1x32_kernel<__nv_bfloat16><<<grid, 256, 0, as_stream(stream)>>>(
+        static_cast<const __nv_bfloat16*>(x), R, K, ldx, q, ldq, sf, ldsf);
+  else
+    mx_quant_1x32_kernel<float><<<grid, 256, 0, as_stream(stream)>>>(
+        static_cast<const float*>(x), R, K, ldx, q, ldq, sf, ldsf);
+  return launch_status();
+}
+
+fp8bs_status fp8bs_mx_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                           const uint32_t* sfa, int64_t ldsfa, const uint8_t* B, int64_t ldb,
+                           const uint32_t* sfb, int64_t ldsfb, void* C, fp8bs_dtype ct,
+                           int64_t ldc, void* stream) {
+  if (M < 0 || N < 0 || K < 0 || !valid_dtype(ct)) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return FP8BS_OK;
+  if (K % kBK != 0 || N % 16 != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (M > INT_MAX - kBM || N > INT_MAX - kBN || K / kBK > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+  if (((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN) > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+  if (C == nullptr || ldc < N) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned(C, 16) || (ldc * static_cast<int64_t>(dtype_size(ct))) % 16 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  if (K == 0) return zero_fill(C, ct, M, N, ldc, as_stream(stream));
+  if (A == nullptr || B == nullptr || sfa == nullptr || sfb == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldsfa < M || ldsfb < N) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || lda % 16 != 0 || ldb % 16 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  if (!aligned(sfa, 16) || !aligned(sfb, 16) || ldsfa % 4 != 0 || ldsfb % 4 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  DeviceInfo di;
+  fp8bs_status st = device_info(&di);
+  if (st != FP8BS_OK) return st;
+  CUtensorMap ta, tb, tsa, tsb, tc;
+  const int64_t KB = K / kBK;
+  if ((st = make_map_2d(&ta, A, K, M, lda, kBM)) != FP8BS_OK) return st;
+  if ((st = make_map_2d(&tb, B, K, N, ldb, kBN)) != FP8BS_OK) return st;
+  if ((st = make_map_sf(&tsa, sfa, M, KB, ldsfa, kBM)) != FP8BS_OK) return st;
+  if ((st = make_map_sf(&tsb, sfb, N, KB, ldsfb, kBN)) != FP8BS_OK) return st;
+  if ((st = make_map_out(&tc, C, ct, N, M, ldc)) != FP8BS_OK) return st;
+  MxParams p{};
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(N);
+  p.KB = static_cast<int32_t>(KB);
+  p.num_m_tiles = static_cast<int32_t>((M + kBM - 1) / kBM);
+  p.num_n_tiles = static_cast<int32_t>((N + kBN - 1) / kBN);
+  const int tiles = p.num_m_tiles * p.num_n_tiles;
+  const int grid = tiles < di.num_sms ? tiles : di.num_sms;
+  auto run = [&](auto kernel) -> fp8bs_status {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kMxSmemBytes)) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
+    kernel<<<grid, kMxThreads, kMxSmemBytes, as_stream(stream)>>>(p, ta, tb, tsa, tsb, tc);
+    return launch_status();
+  };
+  return ct == FP8BS_BF16 ? run(fp8bs_mx_gemm_kernel<true>) : run(fp8bs_mx_gemm_kernel<false>);
 }
 
 fp8bs_status fp8bs_debug_timeout_probe(int64_t limit_ns, void* stream) {

@@ -407,4 +407,49 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n) {
          | ((m >> 4) << 24);  // M / 16
 }
 
+// ------------------------------------------------ block-scaled MMA (MX variant)
+
+// D[tmem] (+)= (A * B^T) with per-32-deep-group power-of-two scales applied
+// by the tensor core: A, B E4M3 in shared memory, one UE8M0 scale per row of
+// A and per row of B for this K=32 step, read from TMEM at sfa_tmem / sfb_tmem
+// (byte `sf id` of each 32-bit cell, the id carried in idesc).  One thread.
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with UE8M0 scales: A = B = E4M3,
+// both K-major, D = F32; sf_id picks the byte of each scale cell for both
+// operands.
+//   bits 4-5 B scale id   7-9 A format   10-12 B format   17-22 N / 8
+//   bit 23 scale type (1 = UE8M0)   24-28 M / 16   29-30 A scale id
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(uint32_t m, uint32_t n, uint32_t sf_id) {
+  return (sf_id << 4) | (0u << 7) | (0u << 10) | ((n >> 3) << 17) | (1u << 23) |
+         ((m >> 4) << 24) | (sf_id << 29);
+}
+
+// Whole warp: 32 lanes (the warp's quadrant) x 4 / 8 consecutive 32-bit
+// columns from registers (thread i -> lane base + i).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 }  // namespace fp8bs

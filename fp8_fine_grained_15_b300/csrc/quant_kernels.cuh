@@ -645,4 +645,82 @@ __global__ void dispatch_pad_kernel(const int32_t* __restrict__ counts,
   }
 }
 
+// ------------------------------------------------------------ MX 1 x 32
+// Microscaling variant ("Should Fixing Deepseek Take 60 Steps?", Figure 7 (a)
+// passage and the page at why-be.why-be.co.kr, accumulation-precision passage:
+// group scaling by the tensor cores is where fine-grained quantization goes
+// next).  Groups of 32 along K; a group's scale is the power of two 2^e with
+// the smallest e such that amax <= 448 * 2^e, clamped to [-127, 127] (0 for an
+// all-zero group), stored as the UE8M0 byte e + 127; code = cvt.rn.satfinite
+// E4M3(x * 2^-e).  The four bytes of a row inside one 128-wide K block form
+// one 32-bit word (group 4kb + j in byte j), words at sf[kb * ldsf + row].
+
+// e for a group with max-abs amax.  amax = (1 + m / 2^23) * 2^E for a normal
+// amax and 448 = 1.75 * 2^8, so e = E - 8 when the significand is at most
+// 1.75 and E - 7 above it; a subnormal amax is below 448 * 2^-127 and clamps.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  if (amax == 0.0f) return 0;
+  const uint32_t bits = __float_as_uint(amax);
+  const int biased = static_cast<int>(bits >> 23);
+  if (biased == 0) return -127;
+  const int e = biased - 127 - 8 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : e;   // e <= 120 for any finite amax
+}
+
+// One warp per row and 1024-column chunk (lane l: the 32 columns of group l,
+// 64 or 128 contiguous bytes), 8 rows per CTA.  The exponent words of the 8
+// rows are gathered in shared memory and written as 32-byte runs.
+template <typename TIn>
+__global__ void __launch_bounds__(256) mx_quant_1x32_kernel(const TIn* __restrict__ x, int64_t R,
+                                                            int64_t K, int64_t ldx,
+                                                            uint8_t* __restrict__ q, int64_t ldq,
+                                                            uint32_t* __restrict__ sf,
+                                                            int64_t ldsf) {
+  constexpr int kV = Vec16<TIn>::kN;       // elements per 16-byte load
+  constexpr int kLoads = 32 / kV;
+  __shared__ uint32_t words[8][8];         // [128-column block of the chunk][row of the CTA]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  const int64_t col = static_cast<int64_t>(blockIdx.y) * 1024 + lane * 32;
+  uint32_t ebyte = 0;
+  if (r < R && col < K) {
+    const TIn* src = x + r * ldx + col;
+    uint4 v[kLoads];
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) v[i] = ld_stream16(src + i * kV);
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) {
+      float w[kV];
+      Vec16<TIn>::widen(v[i], w);
+#pragma unroll
+      for (int j = 0; j < kV; ++j) f[i * kV + j] = w[j];
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    const int e = mx_exponent(amax);
+    const float mult = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e, exact
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = e4m3x4(f + 4 * j, mult);
+    uint4* dst = reinterpret_cast<uint4*>(q + r * ldq + col);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    ebyte = static_cast<uint32_t>(e + 127);
+  }
+  // lanes 4j .. 4j+3 hold the four groups of 128-column block j
+  const uint32_t b1 = __shfl_down_sync(0xffffffffu, ebyte, 1);
+  const uint32_t b2 = __shfl_down_sync(0xffffffffu, ebyte, 2);
+  const uint32_t b3 = __shfl_down_sync(0xffffffffu, ebyte, 3);
+  if ((lane & 3) == 0) words[lane >> 2][warp] = ebyte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    const int kbl = threadIdx.x >> 3, rr = threadIdx.x & 7;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + rr;
+    const int64_t kb = static_cast<int64_t>(blockIdx.y) * 8 + kbl;
+    if (row < R && kb * 128 < K) sf[kb * ldsf + row] = words[kbl][rr];
+  }
+}
+
 }  // namespace fp8bs

@@ -265,6 +265,47 @@ fp8bs_status fp8bs_grouped_gemm(int32_t E, const int32_t* offsets, int64_t M_cap
                                 fp8bs_bscale sb_mode, int64_t ldsb, int64_t sb_estride,
                                 void* C, fp8bs_dtype ct, int64_t ldc, void* stream);
 
+/* MX (microscaling) quantizer: 1x32 groups along K with power-of-two scales
+ * ("Should Fixing Deepseek Take 60 Steps?", Figure 7 (a) passage, and the page
+ * at why-be.why-be.co.kr, accumulation-precision passage: both point to
+ * microscaling, with the group scales applied inside the tensor cores, as the
+ * next step after 1x128 / 128x128 scaling).
+ *   x   [R x K] fp32 or bf16, row stride ldx elements (device);
+ *   q   [R x K] E4M3 codes, row stride ldq bytes (device, caller-owned);
+ *   sf  exponent words (device, caller-owned): for row r and 128-wide K block
+ *       kb, sf[kb*ldsf + r] holds the UE8M0 exponents (e + 127) of the groups
+ *       4kb .. 4kb+3 of that row in bytes 0..3.
+ * A group with max-abs amax gets the smallest e with amax <= 448 * 2^e,
+ * clamped to [-127, 127] (e = 0 for an all-zero group); its codes are
+ * E4M3(fl32(x * 2^-e)) rounded to nearest even with saturation.
+ * Requirements: K % 128 == 0 (UNSUPPORTED); ldx, ldq >= K and ldsf >= R
+ * (INVALID_ARG); x, q 16-byte aligned, ldx*sizeof(xt) and ldq multiples of 16,
+ * sf 4-byte aligned (MISALIGNED; fp8bs_mx_gemm wants sf 16-byte aligned and
+ * ldsf % 4 == 0).  R == 0 or K == 0 is a no-op.  One launch on the stream. */
+fp8bs_status fp8bs_mx_quant_1x32(const void* x, fp8bs_dtype xt, int64_t R, int64_t K, int64_t ldx,
+                                 uint8_t* q, int64_t ldq, uint32_t* sf, int64_t ldsf,
+                                 void* stream);
+
+/* MX GEMM: C[M x N] = sum over 32-deep K groups g of
+ *   ( sum_{k in g} dec(A[m][k]) * dec(B[n][k]) ) * 2^(ea(m,g) + eb(n,g))
+ * with the group exponents applied by the tensor cores (tcgen05 block-scaled
+ * MMA), FP32 accumulation over all of K, BF16 (round to nearest even) or
+ * FP32 output.  Same passages as fp8bs_mx_quant_1x32.
+ *   A [M x K] codes (lda), B [N x K] codes (ldb), both K contiguous (device);
+ *   sfa / sfb exponent words of A's and B's rows in the layout that
+ *   fp8bs_mx_quant_1x32 writes (ldsfa >= M, ldsfb >= N);
+ *   C [M x N] row-major, ldc elements (device, caller-owned).
+ * Requirements: K % 128 == 0 and N % 16 == 0 (UNSUPPORTED); leading
+ * dimensions as above (INVALID_ARG); A, B, C, sfa, sfb 16-byte aligned, lda
+ * and ldb multiples of 16, ldc*sizeof(ct) a multiple of 16, ldsfa and ldsfb
+ * multiples of 4 (MISALIGNED).  M == 0 or N == 0: no-op; K == 0: C = 0.
+ * Asynchronous on the stream; allocates nothing; fp8bs_sync_status reports a
+ * device-side timeout. */
+fp8bs_status fp8bs_mx_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                           const uint32_t* sfa, int64_t ldsfa, const uint8_t* B, int64_t ldb,
+                           const uint32_t* sfb, int64_t ldsfb, void* C, fp8bs_dtype ct,
+                           int64_t ldc, void* stream);
+
 /* Synchronize the stream, then report (and clear) the device error word of the
  * current device: FP8BS_ERR_DEVICE_TIMEOUT, FP8BS_ERR_DEVICE_BAD_ROUTING,
  * FP8BS_ERR_DEVICE_BAD_OFFSETS (in that order of precedence), FP8BS_ERR_CUDA

@@ -147,3 +147,37 @@ def test_dispatch_host_checks(L):
     assert L.fp8bs_quant_dispatch(*args(4, 1024, K=100)) == fb.FP8BS_ERR_UNSUPPORTED
     assert L.fp8bs_quant_dispatch(*args(4, 512)) == fb.FP8BS_ERR_INVALID_ARG         # < T + 127 E
     assert L.fp8bs_quant_dispatch(*args(4, 1000)) == fb.FP8BS_ERR_UNSUPPORTED        # M_cap % 128
+
+
+def _mx_gemm(L, M=128, N=256, K=256, A=FAKE, lda=256, sfa=FAKE, ldsfa=128, B=FAKE, ldb=256,
+             sfb=FAKE, ldsfb=256, C=FAKE, ct=BF16, ldc=256):
+    return L.fp8bs_mx_gemm(M, N, K, A, lda, sfa, ldsfa, B, ldb, sfb, ldsfb, C, ct, ldc, None)
+
+
+def test_mx_gemm_host_checks(L):
+    assert _mx_gemm(L, K=100) == fb.FP8BS_ERR_UNSUPPORTED
+    assert _mx_gemm(L, N=200, ldsfb=200, ldc=200) == fb.FP8BS_ERR_UNSUPPORTED      # N % 16
+    assert _mx_gemm(L, ct=5) == fb.FP8BS_ERR_INVALID_ARG
+    assert _mx_gemm(L, A=NULL) == fb.FP8BS_ERR_INVALID_ARG
+    assert _mx_gemm(L, sfb=NULL) == fb.FP8BS_ERR_INVALID_ARG
+    assert _mx_gemm(L, lda=128) == fb.FP8BS_ERR_INVALID_ARG
+    assert _mx_gemm(L, ldsfa=64) == fb.FP8BS_ERR_INVALID_ARG
+    assert _mx_gemm(L, ldsfb=128) == fb.FP8BS_ERR_INVALID_ARG
+    assert _mx_gemm(L, M=130, ldsfa=130) == fb.FP8BS_ERR_MISALIGNED               # ldsfa % 4
+    assert _mx_gemm(L, sfa=FAKE_ODD) == fb.FP8BS_ERR_MISALIGNED
+    assert _mx_gemm(L, lda=264) == fb.FP8BS_ERR_MISALIGNED
+    assert _mx_gemm(L, ldc=260) == fb.FP8BS_ERR_MISALIGNED
+    assert _mx_gemm(L, M=0) == fb.FP8BS_OK
+    assert _mx_gemm(L, M=-1) == fb.FP8BS_ERR_INVALID_ARG
+
+
+def test_mx_quant_host_checks(L):
+    q = L.fp8bs_mx_quant_1x32
+    assert q(NULL, BF16, 4, 100, 100, NULL, 100, NULL, 4, None) == fb.FP8BS_ERR_UNSUPPORTED
+    assert q(NULL, 9, 4, 128, 128, NULL, 128, NULL, 4, None) == fb.FP8BS_ERR_INVALID_ARG
+    assert q(FAKE, BF16, 4, 128, 128, NULL, 128, FAKE, 4, None) == fb.FP8BS_ERR_INVALID_ARG
+    assert q(FAKE, BF16, 4, 128, 128, FAKE, 128, FAKE, 2, None) == fb.FP8BS_ERR_INVALID_ARG
+    assert q(FAKE, BF16, 4, 128, 132, FAKE, 128, FAKE, 4, None) == fb.FP8BS_ERR_MISALIGNED
+    assert q(FAKE, BF16, 4, 128, 128, FAKE, 136, FAKE, 4, None) == fb.FP8BS_ERR_MISALIGNED
+    assert q(FAKE, BF16, 4, 128, 128, FAKE, 128, FAKE + 2, 4, None) == fb.FP8BS_ERR_MISALIGNED
+    assert q(NULL, BF16, 0, 128, 128, NULL, 128, NULL, 0, None) == fb.FP8BS_OK
