@@ -429,6 +429,27 @@ def run_extras(dev, stream, peaks):
                                  "launches": 4}
     del xt, qd, sd
 
+    # MX variant: the layer's Fprop with 1x32 power-of-two scales applied by the
+    # tensor cores, and the MX quantizer of X
+    xm = torch.randn((TOKENS, HIDDEN), device=dev, generator=gen).to(torch.bfloat16)
+    wm = (torch.randn((FFN, HIDDEN), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+    Am = torch.empty((TOKENS, HIDDEN), dtype=torch.uint8, device=dev)
+    Bm = torch.empty((FFN, HIDDEN), dtype=torch.uint8, device=dev)
+    sfa = torch.empty((HIDDEN // 128, TOKENS), dtype=torch.int32, device=dev)
+    sfb = torch.empty((HIDDEN // 128, FFN), dtype=torch.int32, device=dev)
+    fb.fp8bs_mx_quant_1x32(wm, Bm, sfb, stream)
+    mq, _ = timeit(lambda: fb.fp8bs_mx_quant_1x32(xm, Am, sfa, stream), flush=flush)
+    Cm = torch.empty((TOKENS, FFN), dtype=torch.bfloat16, device=dev)
+    mg, _ = timeit(lambda: fb.fp8bs_mx_gemm(Am, sfa, Bm, sfb, Cm, stream), flush=flush)
+    qbytes = quant_bytes(TOKENS * HIDDEN, 2)
+    flops = 2.0 * TOKENS * HIDDEN * FFN
+    out["mx_variant"] = {
+        "fprop_ms": round(mg, 4), "fprop_TFLOP/s": round(flops / (mg * 1e-3) / 1e12, 1),
+        "fprop_frac_fp8_peak": round(flops / (mg * 1e-3) / 1e12 / peaks["fp8_tflops"], 4),
+        "quant_X_us": round(mq * 1e3, 2), "quant_X_GB/s": round(qbytes / (mq * 1e-3) / 1e9, 1),
+        "quant_X_frac_hbm": round(qbytes / (mq * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    del xm, wm, Am, Bm, sfa, sfb, Cm
+
     # quantizer sweep
     sweep = {}
     for M in (1024, 8192, 65536):
@@ -528,7 +549,7 @@ def run_reference(args, rank, world, dist_on):
 
 
 CASES = ("fprop", "dgrad", "wgrad", "grouped", "quant_1x128", "quant_128x1", "quant_dual",
-         "quant_128x128")
+         "quant_128x128", "mx_fprop", "mx_quant")
 
 
 def run_case(args):
@@ -571,6 +592,18 @@ def run_case(args):
         ws = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
         fn = lambda: fb.fp8bs_gemm_ws(A, sa, B, sb, mode, out, ws, stream)  # noqa: E731
         amount, kind = 2.0 * T * K * N, "tensor"
+    elif c == "mx_fprop":
+        x = torch.randn((T, K), device=dev, generator=gen).to(torch.bfloat16)
+        w = (torch.randn((N, K), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+        A, B = u8(T, K), u8(N, K)
+        sfa = torch.empty((K // 128, T), dtype=torch.int32, device=dev)
+        sfb = torch.empty((K // 128, N), dtype=torch.int32, device=dev)
+        fb.fp8bs_mx_quant_1x32(x, A, sfa, stream)
+        fb.fp8bs_mx_quant_1x32(w, B, sfb, stream)
+        del x, w
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fb.fp8bs_mx_gemm(A, sfa, B, sfb, out, stream)  # noqa: E731
+        amount, kind = 2.0 * T * K * N, "tensor"
     elif c == "grouped":
         counts = wl.zipf_counts()
         offsets = wl.padded_offsets(counts)
@@ -601,6 +634,10 @@ def run_case(args):
             elif c == "quant_128x1":
                 q, s = u8(K, M), f32(M // 128, K)
                 fn = lambda: fb.fp8bs_quant_act_128x1(x, q, s, stream)  # noqa: E731
+            elif c == "mx_quant":
+                q = u8(M, K)
+                s = torch.empty((K // 128, M), dtype=torch.int32, device=dev)
+                fn = lambda: fb.fp8bs_mx_quant_1x32(x, q, s, stream)  # noqa: E731
             else:
                 q, s, qT, sT = u8(M, K), f32(K // 128, M), u8(K, M), f32(M // 128, K)
                 fn = lambda: fb.fp8bs_quant_act_dual(x, q, s, qT, sT, stream)  # noqa: E731
