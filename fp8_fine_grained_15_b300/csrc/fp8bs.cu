@@ -315,10 +315,10 @@ fp8bs_status launch_gemm_pair(GemmParams& p, const CUtensorMap& ta, const CUtens
               : run(fp8bs_gemm_pair_kernel<BN, kSbPerCol, false>);
 }
 
-template <bool kGrouped>
-fp8bs_status launch_gemm(GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                         const CUtensorMap& tc, int sb_kind, fp8bs_dtype ct,
-                         cudaStream_t stream) {
+// Launch of the single-CTA grouped GEMM: one persistent CTA per SM (at most one per tile).
+fp8bs_status launch_grouped(GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                            const CUtensorMap& tc, int sb_kind, fp8bs_dtype ct,
+                            cudaStream_t stream) {
   DeviceInfo di;
   fp8bs_status st = device_info(&di);
   if (st != FP8BS_OK) return st;
@@ -333,10 +333,10 @@ fp8bs_status launch_gemm(GemmParams& p, const CUtensorMap& ta, const CUtensorMap
   };
   const bool bf16 = ct == FP8BS_BF16;
   if (sb_kind == kSbBlock)
-    return bf16 ? run(fp8bs_gemm_kernel<kGrouped, kSbBlock, true>)
-                : run(fp8bs_gemm_kernel<kGrouped, kSbBlock, false>);
-  return bf16 ? run(fp8bs_gemm_kernel<kGrouped, kSbPerCol, true>)
-              : run(fp8bs_gemm_kernel<kGrouped, kSbPerCol, false>);
+    return bf16 ? run(fp8bs_gemm_kernel<kSbBlock, true>)
+                : run(fp8bs_gemm_kernel<kSbBlock, false>);
+  return bf16 ? run(fp8bs_gemm_kernel<kSbPerCol, true>)
+              : run(fp8bs_gemm_kernel<kSbPerCol, false>);
 }
 
 void fill_scale_strides(GemmParams& p, fp8bs_bscale mode, int64_t ldsb) {
@@ -705,8 +705,8 @@ fp8bs_status fp8bs_grouped_gemm(int32_t E, const int32_t* offsets, int64_t M_cap
   p.C = C;
   p.ldc = ldc;
   p.offsets = offsets;
-  return launch_gemm<true>(p, ta, tb, tc, sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct,
-                           as_stream(stream));
+  return launch_grouped(p, ta, tb, tc, sb_mode == FP8BS_SB_PERCOL ? kSbPerCol : kSbBlock, ct,
+                        as_stream(stream));
 }
 
 fp8bs_status fp8bs_sync_status(void* stream) {

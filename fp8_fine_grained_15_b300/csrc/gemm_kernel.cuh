@@ -8,6 +8,12 @@
 // cores with the scales applied; MMA and promotion overlap so the tensor cores
 // stay busy).
 //
+// This single-CTA kernel serves the grouped (MoE expert) GEMM, whose experts
+// are padded to 128 rows: a 256-row pair tile would straddle two experts, and
+// the pair form that loads zeros for such halves measured slower (its
+// block-scale promotion spills at the register limit).  The dense GEMM runs on
+// the CTA-pair kernel (gemm_pair_kernel.cuh), which reuses the helpers here.
+//
 // B300 design (one CTA per SM, persistent):
 //   warp 0      TMA producer: A tile 128x128 B and B tile 256x128 B per K-slab,
 //               128-byte swizzle, into a kStages-deep shared-memory ring.
@@ -105,30 +111,22 @@ struct TileCoord {
   int32_t m0, n0, e;
 };
 
-// Output tile t of the persistent walk.  Dense: m tiles fastest, so the CTAs
-// of one wave share a few B panels and all of A stays in L2.  Grouped: expert
-// by expert, and within an expert its m tiles fastest, so an expert's rows of
-// A are re-read from L2 across its n tiles instead of from HBM.
-template <bool kGrouped>
+// Output tile t of the persistent walk: expert by expert, and within an
+// expert its m tiles fastest, so an expert's rows of A are re-read from L2
+// across its n tiles instead of from HBM.
 __device__ __forceinline__ TileCoord tile_coord(int t, const GemmParams& p, const GemmSmem& sm) {
   TileCoord c;
-  if constexpr (kGrouped) {
-    // owner: the last e with tile_base[e] <= t (it has at least one tile)
-    int lo = 0, hi = p.E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (sm.tile_base[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    const int l = t - sm.tile_base[lo];
-    const int mte = (sm.offsets[lo + 1] - sm.offsets[lo]) / kBM;
-    c.e = lo;
-    c.m0 = sm.offsets[lo] + (l % mte) * kBM;
-    c.n0 = (l / mte) * kBN;
-  } else {
-    c.e = 0;
-    c.m0 = (t % p.num_m_tiles) * kBM;
-    c.n0 = (t / p.num_m_tiles) * kBN;
+  // owner: the last e with tile_base[e] <= t (it has at least one tile)
+  int lo = 0, hi = p.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sm.tile_base[mid] <= t) lo = mid; else hi = mid - 1;
   }
+  const int l = t - sm.tile_base[lo];
+  const int mte = (sm.offsets[lo + 1] - sm.offsets[lo]) / kBM;
+  c.e = lo;
+  c.m0 = sm.offsets[lo] + (l % mte) * kBM;
+  c.n0 = (l / mte) * kBN;
   return c;
 }
 
@@ -204,7 +202,7 @@ __device__ __forceinline__ void store_rows_tma(const float2* acc, uint32_t stg, 
   }
 }
 
-template <bool kGrouped, int kSb, bool kOutBf16>
+template <int kSb, bool kOutBf16>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fp8bs_gemm_kernel(const __grid_constant__ GemmParams p,
                       const __grid_constant__ CUtensorMap tmap_a,
@@ -239,7 +237,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmap_b);
     tma_prefetch_desc(&tmap_c);
   }
-  if constexpr (kGrouped) {
+  {
     // Stage and validate the expert offsets (every CTA, so none depends on another).
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) sm.offsets[i] = p.offsets[i];
     __syncthreads();
@@ -283,10 +281,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sm.tmem_base;
-  const bool skip_all = kGrouped && sm.bad_offsets;
+  const bool skip_all = sm.bad_offsets != 0;
   // (re-read per tile rather than held in a register: the promotion warps
   // have none to spare)
-#define FP8BS_NUM_TILES (kGrouped ? sm.num_tiles : p.num_m_tiles * p.num_n_tiles)
+#define FP8BS_NUM_TILES (sm.num_tiles)
 
   if (warp < 4) {
     regs_dealloc<kProducerRegs>();
@@ -297,7 +295,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     uint32_t issued_mask = 0, parity_mask = 0;
     for (int t = blockIdx.x; t < FP8BS_NUM_TILES; t += gridDim.x) {
-      const TileCoord tc = tile_coord<kGrouped>(t, p, sm);
+      const TileCoord tc = tile_coord(t, p, sm);
       for (int kb = 0; kb < p.KB; ++kb) {
         if (!bounded_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) goto producer_done;
         mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
@@ -325,7 +323,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0, tphase = 0;
     bool issued = false;
     for (int t = blockIdx.x; t < FP8BS_NUM_TILES; t += gridDim.x) {
-      const TileCoord tc = tile_coord<kGrouped>(t, p, sm);
+      const TileCoord tc = tile_coord(t, p, sm);
       for (int kb = 0; kb < p.KB; ++kb) {
         if (!bounded_wait(&sm.full[stage], phase, abort_flag)) goto mma_done;
         if (!bounded_wait(&sm.tempty[buf], tphase ^ 1u, abort_flag)) goto mma_done;
@@ -365,7 +363,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int buf = 0;
     uint32_t tphase = 0;
     for (int t = blockIdx.x; t < FP8BS_NUM_TILES; t += gridDim.x) {
-      const TileCoord tc = tile_coord<kGrouped>(t, p, sm);
+      const TileCoord tc = tile_coord(t, p, sm);
       const int row = tc.m0 + g * 32 + lane;
       const bool row_ok = row < p.M;
       const int col0 = tc.n0 + h * 128;
