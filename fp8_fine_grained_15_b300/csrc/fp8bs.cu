@@ -492,16 +492,19 @@ fp8bs_status fp8bs_quant_act_128x1(const void* x, fp8bs_dtype xt, int64_t T, int
     return FP8BS_ERR_MISALIGNED;
   const int64_t cb = xt == FP8BS_BF16 ? 128 : 64;
   dim3 grid(static_cast<unsigned>((C + cb - 1) / cb), static_cast<unsigned>(T / 128));
-  if (xt == FP8BS_BF16) {
-    prefer_max_shared(quant_128x1_kernel<__nv_bfloat16>);
-    quant_128x1_kernel<__nv_bfloat16><<<grid, 256, 0, as_stream(stream)>>>(
-        static_cast<const __nv_bfloat16*>(x), C, ldx, qT, ldq, s, lds);
-  } else {
-    prefer_max_shared(quant_128x1_kernel<float>);
-    quant_128x1_kernel<float><<<grid, 256, 0, as_stream(stream)>>>(static_cast<const float*>(x),
-                                                                   C, ldx, qT, ldq, s, lds);
-  }
-  return launch_status();
+  auto run = [&](auto kernel, size_t smem, auto* xin) -> fp8bs_status {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
+    prefer_max_shared(kernel);
+    kernel<<<grid, 256, smem, as_stream(stream)>>>(xin, C, ldx, qT, ldq, s, lds);
+    return launch_status();
+  };
+  if (xt == FP8BS_BF16)
+    return run(quant_128x1_kernel<__nv_bfloat16>, quant_128x1_smem_bytes<__nv_bfloat16>(),
+               static_cast<const __nv_bfloat16*>(x));
+  return run(quant_128x1_kernel<float>, quant_128x1_smem_bytes<float>(),
+             static_cast<const float*>(x));
 }
 
 fp8bs_status fp8bs_quant_act_dual(const void* x, fp8bs_dtype xt, int64_t T, int64_t C,
@@ -519,8 +522,13 @@ fp8bs_status fp8bs_quant_act_dual(const void* x, fp8bs_dtype xt, int64_t T, int6
       ldq % 16 || !aligned(qT, 16) || ldqT % 16 || !aligned(s, 4) || !aligned(sT, 4))
     return FP8BS_ERR_MISALIGNED;
   dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(T / 128));
-  const size_t smem = 128 * 128 * dtype_size(xt);
+  // staged input tile + the transposed codes (128 x 128 bytes)
+  const size_t smem = 128 * 128 * dtype_size(xt) + 128 * 128;
   if (xt == FP8BS_BF16) {
+    if (cudaFuncSetAttribute(quant_dual_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
     prefer_max_shared(quant_dual_kernel<__nv_bfloat16>);
     quant_dual_kernel<__nv_bfloat16><<<grid, 256, smem, as_stream(stream)>>>(
         static_cast<const __nv_bfloat16*>(x), ldx, q, ldq, s, lds, qT, ldqT, sT, ldsT);

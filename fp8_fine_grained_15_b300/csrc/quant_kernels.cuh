@@ -168,7 +168,29 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const TIn* __restrict_
 // channel) and 32 consecutive tokens: 32 conflict-free word reads, a
 // per-channel partial amax combined across the four token parts through shared
 // memory, then 32 codes per channel (words re-read from shared memory) written
-// as two 16-byte runs of the transposed output.
+// as two 16-byte chunks of that channel's 128-byte output row, staged in
+// shared memory (chunk j of row c at j ^ ((c / channels-per-word) & 7):
+// conflict-free for the writers).  Eight consecutive lanes then store each
+// whole row, so every warp store covers four complete 128-byte lines.
+template <typename TIn>
+constexpr size_t quant_128x1_smem_bytes() {
+  return 128 * 64 * 4 /* staged tile: 128 tokens x 64 words */ +
+         (256 / sizeof(TIn)) * 128 /* transposed codes: channels x 128 tokens */;
+}
+
+// Coalesced store of staged transposed codes: rows [0, rows) of 128 bytes,
+// chunk j of row c at position j ^ ((c / kCh) & 7), to dst_row(c) + 16 j.
+template <int kCh>
+__device__ __forceinline__ void store_transposed_rows(const uint4* outT, int rows, int64_t c_limit,
+                                                      uint8_t* base, int64_t ld) {
+  for (int i = threadIdx.x; i < rows * 8; i += blockDim.x) {
+    const int c = i >> 3, j = i & 7;
+    if (c < c_limit)
+      *reinterpret_cast<uint4*>(base + static_cast<int64_t>(c) * ld + j * 16) =
+          outT[c * 8 + (j ^ ((c / kCh) & 7))];
+  }
+}
+
 template <typename TIn>
 __global__ void __launch_bounds__(256, 4) quant_128x1_kernel(const TIn* __restrict__ x, int64_t C,
                                                              int64_t ldx, uint8_t* __restrict__ qT,
@@ -183,7 +205,10 @@ __global__ void __launch_bounds__(256, 4) quant_128x1_kernel(const TIn* __restri
   constexpr int kGroups = kCB / kCh;           // 64 word columns
   constexpr int kParts = 256 / kGroups;        // 4 token parts
   constexpr int kTok = 128 / kParts;           // 32 tokens per thread
-  __shared__ __align__(16) uint32_t tile[128][kGroups];
+  static_assert(kGroups == 64 && kTok == 32, "layout of quant_128x1_smem_bytes");
+  extern __shared__ __align__(16) unsigned char q128x1_smem[];
+  uint32_t (*tile)[kGroups] = reinterpret_cast<uint32_t (*)[kGroups]>(q128x1_smem);
+  uint4* outT = reinterpret_cast<uint4*>(q128x1_smem + 128 * kGroups * 4);   // [kCB][8]
   __shared__ float part_amax[kParts][kCB];
 
   const int64_t tb = blockIdx.y;
@@ -234,27 +259,27 @@ __global__ void __launch_bounds__(256, 4) quant_128x1_kernel(const TIn* __restri
     for (int p = 1; p < kParts; ++p) a = fmaxf(a, part_amax[p][g * kCh + k]);
     float sc, r;
     tile_scale(a, sc, r);
-    const int64_t c = c0 + g * kCh + k;
-    if (c < C) {
-      uint8_t* dst = qT + c * ldq + tb * 128 + part * kTok;
+    const int cl = g * kCh + k;   // channel within the CTA's block
 #pragma unroll 1
-      for (int t = 0; t < kTok; t += 16) {   // words re-read from shared memory (no spills)
-        uint32_t o[4];
+    for (int t = 0; t < kTok; t += 16) {   // words re-read from shared memory (no spills)
+      uint32_t o[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float f[4];
+      for (int j = 0; j < 4; ++j) {
+        float f[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t wv = tile[part * kTok + t + 4 * j + i][g];
-            f[i] = __uint_as_float(kCh == 1 ? wv : (k == 0 ? (wv << 16) : (wv & 0xFFFF0000u)));
-          }
-          o[j] = e4m3x4(f, r);
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t wv = tile[part * kTok + t + 4 * j + i][g];
+          f[i] = __uint_as_float(kCh == 1 ? wv : (k == 0 ? (wv << 16) : (wv & 0xFFFF0000u)));
         }
-        *reinterpret_cast<uint4*>(dst + t) = make_uint4(o[0], o[1], o[2], o[3]);
+        o[j] = e4m3x4(f, r);
       }
-      if (part == 0) s[tb * lds + c] = sc;
+      const int chunk = (part * kTok + t) >> 4;
+      outT[cl * 8 + (chunk ^ (g & 7))] = make_uint4(o[0], o[1], o[2], o[3]);
     }
+    if (part == 0 && c0 + cl < C) s[tb * lds + c0 + cl] = sc;
   }
+  __syncthreads();
+  store_transposed_rows<kCh>(outT, kCB, C - c0, qT + c0 * ldq + tb * 128, ldq);
 }
 
 // -------------------------------------------------------------- 128 x 128
@@ -388,6 +413,9 @@ __global__ void __launch_bounds__(256) quant_dual_kernel(const TIn* __restrict__
   constexpr int kRows = 128 / kParts;                       // 32 or 64 tokens per thread
   extern __shared__ __align__(16) unsigned char dual_smem[];
   uint32_t* tile = reinterpret_cast<uint32_t*>(dual_smem);  // [128][kWordsPerRow], swizzled
+  // transposed codes [128 channels][8 chunks of 16 tokens], chunk j of channel c
+  // at j ^ ((c / kCh) & 7), stored as whole 128-byte rows at the end
+  uint4* outT = reinterpret_cast<uint4*>(dual_smem + 128 * kWordsPerRow * 4);
   __shared__ float part_amax[kParts][128];
 
   const int64_t tb = blockIdx.y, cb = blockIdx.x;
@@ -478,7 +506,6 @@ __global__ void __launch_bounds__(256) quant_dual_kernel(const TIn* __restrict__
     for (int p2 = 1; p2 < kParts; ++p2) a = fmaxf(a, part_amax[p2][c]);
     float sc, r;
     tile_scale(a, sc, r);
-    uint8_t* dst = qT + (cb * 128 + c) * ldqT + tb * 128 + part * kRows;
 #pragma unroll 1
     for (int t = 0; t < kRows; t += 16) {
       uint32_t o[4];
@@ -492,10 +519,13 @@ __global__ void __launch_bounds__(256) quant_dual_kernel(const TIn* __restrict__
         }
         o[j] = e4m3x4(f, r);
       }
-      *reinterpret_cast<uint4*>(dst + t) = make_uint4(o[0], o[1], o[2], o[3]);
+      const int chunk = (part * kRows + t) >> 4;
+      outT[c * 8 + (chunk ^ (g & 7))] = make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (part == 0) sT[tb * ldsT + cb * 128 + c] = sc;
   }
+  __syncthreads();
+  store_transposed_rows<kCh>(outT, 128, 128, qT + cb * 128 * ldqT + tb * 128, ldqT);
 }
 
 // ------------------------------------------------ quantize-then-dispatch (MoE)
