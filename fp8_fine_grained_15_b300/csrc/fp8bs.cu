@@ -602,8 +602,13 @@ fp8bs_status fp8bs_quant_w_128x128(const void* w, fp8bs_dtype wt, int64_t R, int
   if (q && (!aligned(q, 16) || ldq % 16)) return FP8BS_ERR_MISALIGNED;
   if (qT && (!aligned(qT, 16) || ldqT % 16)) return FP8BS_ERR_MISALIGNED;
   dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R / 128));
-  const size_t smem = 128 * 128 * dtype_size(wt);
+  // staged block, plus the transposed codes (128 x 128 bytes) when qT is asked for
+  const size_t smem = 128 * 128 * dtype_size(wt) + (qT != nullptr ? 128 * 128 : 0);
   if (wt == FP8BS_BF16) {
+    if (cudaFuncSetAttribute(quant_128x128_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return FP8BS_ERR_CUDA;
     prefer_max_shared(quant_128x128_kernel<__nv_bfloat16>);
     quant_128x128_kernel<__nv_bfloat16><<<grid, 256, smem, as_stream(stream)>>>(
         static_cast<const __nv_bfloat16*>(w), ldw, q, ldq, qT, ldqT, s, lds);

@@ -287,9 +287,11 @@ __global__ void __launch_bounds__(256, 4) quant_128x1_kernel(const TIn* __restri
 // for bf16, 64 KB for fp32).  Each thread owns one 32-bit word column (two
 // bf16 channels or one fp32 channel) over a run of rows: it reduces its part of
 // the block amax from those words (then warp shuffles + shared memory), and
-// later re-reads them 16 rows at a time to write that column's transposed
-// codes.  The row-major codes come from 16-byte shared-memory reads.  Both
-// copies use the same multiply and conversion, so they hold identical codes.
+// later re-reads them 16 rows at a time to form that column's transposed
+// codes, staged as 128-byte output rows in shared memory (swizzled as in the
+// 128x1 kernel) and stored as whole rows by consecutive lanes.  The row-major
+// codes come from 16-byte shared-memory reads.  Both copies use the same
+// multiply and conversion, so they hold identical codes.
 template <typename TIn>
 __global__ void __launch_bounds__(256, 5) quant_128x128_kernel(const TIn* __restrict__ w,
                                                                int64_t ldw,
@@ -307,6 +309,8 @@ __global__ void __launch_bounds__(256, 5) quant_128x128_kernel(const TIn* __rest
   constexpr int kRows = 128 / kParts;                       // 32 or 64 rows per thread
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   uint32_t* tile = reinterpret_cast<uint32_t*>(dyn_smem);   // [128][kWordsPerRow]
+  // with qT: the transposed codes [128 channels][8 chunks of 16 rows]
+  uint4* outT = reinterpret_cast<uint4*>(dyn_smem + 128 * kWordsPerRow * 4);
   __shared__ float warp_amax[8];
 
   const int64_t rb = blockIdx.y, cb = blockIdx.x;
@@ -350,7 +354,6 @@ __global__ void __launch_bounds__(256, 5) quant_128x128_kernel(const TIn* __rest
 
   if (qT != nullptr) {
     // 16 rows at a time: 16 words -> 16 codes for each channel of the word
-    uint8_t* d0 = qT + (cb * 128 + g * kCh) * ldqT + rb * 128 + part * kRows;
 #pragma unroll 1
     for (int t = 0; t < kRows; t += 16) {
       uint32_t v[16];
@@ -369,9 +372,12 @@ __global__ void __launch_bounds__(256, 5) quant_128x128_kernel(const TIn* __rest
           }
           o[j] = e4m3x4(f, r);
         }
-        *reinterpret_cast<uint4*>(d0 + k * ldqT + t) = make_uint4(o[0], o[1], o[2], o[3]);
+        const int chunk = (part * kRows + t) >> 4;
+        outT[(g * kCh + k) * 8 + (chunk ^ (g & 7))] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
+    __syncthreads();
+    store_transposed_rows<kCh>(outT, 128, 128, qT + cb * 128 * ldqT + rb * 128, ldqT);
   }
   if (q != nullptr) {
     uint8_t* dst = q + rb * 128 * ldq + cb * 128;
