@@ -549,7 +549,7 @@ def run_reference(args, rank, world, dist_on):
 
 
 CASES = ("fprop", "dgrad", "wgrad", "grouped", "quant_1x128", "quant_128x1", "quant_dual",
-         "quant_128x128", "mx_fprop", "mx_quant")
+         "quant_128x128", "mx_fprop", "mx_quant", "quant_dispatch")
 
 
 def run_case(args):
@@ -604,6 +604,18 @@ def run_case(args):
         out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
         fn = lambda: fb.fp8bs_mx_gemm(A, sfa, B, sfb, out, stream)  # noqa: E731
         amount, kind = 2.0 * T * K * N, "tensor"
+    elif c == "quant_dispatch":
+        expert = torch.from_numpy(wl.zipf_expert_ids().astype(np.int32)).to(dev)
+        E, T_ = wl.EXPERTS, int(expert.numel())
+        x = torch.randn((T_, K), device=dev, generator=gen).to(torch.bfloat16)
+        Mc = (T_ + 127 * E + 127) // 128 * 128
+        q, s = u8(Mc, K), f32(K // 128, Mc)
+        i32 = lambda n: torch.empty(n, dtype=torch.int32, device=dev)  # noqa: E731
+        offd, cntd, t2r, r2t = i32(E + 1), i32(E), i32(T_), i32(Mc)
+        fn = lambda: fb.fp8bs_quant_dispatch(x, expert, E, q, s, offd, cntd, t2r, r2t,  # noqa: E731
+                                             stream)
+        padded = int(wl.padded_offsets(wl.zipf_counts())[-1])
+        amount, kind = quant_bytes(T_ * K, 2) + (padded - T_) * (K + 4 * K / 128), "hbm"
     elif c == "grouped":
         counts = wl.zipf_counts()
         offsets = wl.padded_offsets(counts)

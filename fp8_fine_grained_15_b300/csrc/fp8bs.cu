@@ -583,7 +583,7 @@ fp8bs_status fp8bs_quant_dispatch(const void* x, fp8bs_dtype xt, int64_t T, int6
   dispatch_rows_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, st>>>(
       expert, T, E, offsets, token_row, row_token);
   if ((rc = launch_status()) != FP8BS_OK) return rc;
-  dispatch_pad_kernel<<<static_cast<unsigned>(E), 256, 0, st>>>(
+  dispatch_pad_kernel<<<dim3(static_cast<unsigned>(E), 127), 256, 0, st>>>(
       counts, offsets, static_cast<int>(K / 128), q, ldq, s, lds, row_token);
   return launch_status();
 }

@@ -546,19 +546,26 @@ constexpr int kDispatchMaxExperts = 256;
 // One CTA of 1024 threads: in chunks of 1024 tokens, each token's rank among
 // the earlier tokens of its expert (warp match + per-warp counts, prefix over
 // warps), then per-expert counts and padded offsets.  rank_out[t] = rank.
+// The per-warp counts are kept expert-major with rows of 33 words
+// (cnt[e][warp]): the prefix over the 32 warps of one expert is a warp-wide
+// shuffle scan of consecutive words, and the per-token rank reads of a warp
+// (one warp column, several experts) fall in different banks.  The next
+// chunk's expert ids are loaded while the current chunk is ranked.
 __global__ void __launch_bounds__(1024) dispatch_plan_kernel(const int32_t* __restrict__ expert,
                                                              int64_t T, int E,
                                                              int32_t* __restrict__ rank_out,
                                                              int32_t* __restrict__ counts,
                                                              int32_t* __restrict__ offsets) {
-  __shared__ int32_t warp_cnt[32][kDispatchMaxExperts];
+  __shared__ int32_t cnt[kDispatchMaxExperts][33];
   __shared__ int32_t running[kDispatchMaxExperts];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int e = tid; e < kDispatchMaxExperts; e += 1024) running[e] = 0;
+  int e_next = tid < T ? expert[tid] : -1;
   for (int64_t base = 0; base < T; base += 1024) {
-    for (int i = tid; i < 32 * kDispatchMaxExperts; i += 1024) (&warp_cnt[0][0])[i] = 0;
+    for (int i = tid; i < 32 * E; i += 1024) cnt[i >> 5][i & 31] = 0;   // rows of the E experts
     const int64_t t = base + tid;
-    int e = t < T ? expert[t] : -1;
+    int e = e_next;
+    e_next = t + 1024 < T ? expert[t + 1024] : -1;
     if (t < T && (e < 0 || e >= E)) {   // routing outside [0, E): the token is dropped
       atomicOr(&g_device_error, kDevErrBadRouting);
       e = -1;
@@ -566,20 +573,23 @@ __global__ void __launch_bounds__(1024) dispatch_plan_kernel(const int32_t* __re
     __syncthreads();
     const unsigned m = __match_any_sync(0xffffffffu, e);
     const int lane_rank = __popc(m & ((1u << lane) - 1u));
-    if (e >= 0 && lane_rank == 0) warp_cnt[warp][e] = __popc(m);
+    if (e >= 0 && lane_rank == 0) cnt[e][warp] = __popc(m);
     __syncthreads();
-    for (int x = tid; x < E; x += 1024) {   // exclusive prefix over the warps, per expert
-      int run = running[x];
-#pragma unroll 4
-      for (int w = 0; w < 32; ++w) {
-        const int c = warp_cnt[w][x];
-        warp_cnt[w][x] = run;
-        run += c;
+    for (int x = warp; x < E; x += 32) {   // exclusive prefix over the warps, per expert
+      const int c = cnt[x][lane];
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
       }
-      running[x] = run;
+      const int run = running[x];
+      cnt[x][lane] = run + incl - c;
+      __syncwarp();
+      if (lane == 31) running[x] = run + incl;
     }
     __syncthreads();
-    if (e >= 0) rank_out[t] = warp_cnt[warp][e] + lane_rank;
+    if (e >= 0) rank_out[t] = cnt[e][warp] + lane_rank;
     __syncthreads();
   }
   if (tid == 0) {
@@ -665,20 +675,20 @@ __global__ void dispatch_rows_kernel(const int32_t* __restrict__ expert, int64_t
   row_token[row] = static_cast<int32_t>(t);
 }
 
-// Padding rows of expert blockIdx.x: codes 0, scales 1, row_token -1.
+// Padding row blockIdx.y of expert blockIdx.x (when the expert has that many
+// padding rows): codes 0, scales 1, row_token -1.
 __global__ void dispatch_pad_kernel(const int32_t* __restrict__ counts,
                                     const int32_t* __restrict__ offsets, int KB,
                                     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s,
                                     int64_t lds, int32_t* __restrict__ row_token) {
   const int e = blockIdx.x;
-  const int64_t r0 = static_cast<int64_t>(offsets[e]) + counts[e], r1 = offsets[e + 1];
-  const int64_t bytes_per_row = static_cast<int64_t>(KB) * 128;
-  for (int64_t r = r0; r < r1; ++r) {
-    uint4* dst = reinterpret_cast<uint4*>(q + r * ldq);
-    for (int64_t i = threadIdx.x; i < bytes_per_row / 16; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
-    for (int kb = threadIdx.x; kb < KB; kb += blockDim.x) s[static_cast<int64_t>(kb) * lds + r] = 1.0f;
-    if (threadIdx.x == 0) row_token[r] = -1;
-  }
+  const int64_t r = static_cast<int64_t>(offsets[e]) + counts[e] + blockIdx.y;
+  if (r >= offsets[e + 1]) return;
+  uint4* dst = reinterpret_cast<uint4*>(q + r * ldq);
+  const int64_t words = static_cast<int64_t>(KB) * 128 / 16;
+  for (int64_t i = threadIdx.x; i < words; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+  for (int kb = threadIdx.x; kb < KB; kb += blockDim.x) s[static_cast<int64_t>(kb) * lds + r] = 1.0f;
+  if (threadIdx.x == 0) row_token[r] = -1;
 }
 
 // ------------------------------------------------------------ MX 1 x 32
