@@ -181,3 +181,12 @@ def test_mx_quant_host_checks(L):
     assert q(FAKE, BF16, 4, 128, 128, FAKE, 136, FAKE, 4, None) == fb.FP8BS_ERR_MISALIGNED
     assert q(FAKE, BF16, 4, 128, 128, FAKE, 128, FAKE + 2, 4, None) == fb.FP8BS_ERR_MISALIGNED
     assert q(NULL, BF16, 0, 128, 128, NULL, 128, NULL, 0, None) == fb.FP8BS_OK
+
+
+def test_binding_wraps_every_declared_function():
+    # the binding's wrappers keep the C names (fp8bs_status_string is status_string)
+    for n in fb.header_functions():
+        if n == "fp8bs_status_string":
+            assert callable(fb.status_string)
+        else:
+            assert callable(getattr(fb, n, None)), f"no Python wrapper for {n}"
