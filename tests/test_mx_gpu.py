@@ -206,3 +206,23 @@ def test_mx_layer_fprop_sampled():
     c_ref, s_abs = oracle.mx_gemm_elements(A, sfa, B, sfb, rows, cols)
     assert_gemm_close(c[rows, cols], c_ref, s_abs, True, "MX Fprop 4096x18432x7168")
     assert np.isfinite(c).all()
+
+
+def test_mx_quant_at_sweep_maximum_sampled():
+    """65536 x 7168 bf16 through the MX quantizer (8192 x 7 CTAs); rows are
+    independent, so 128-row blocks (first, last, random) are compared
+    bit-exactly with the oracle."""
+    x = wl.sweep_activations(65536)
+    R, K = x.shape
+    xd = x.to(DEV)
+    q = torch.empty((R, K), dtype=torch.uint8, device=DEV)
+    sf = torch.empty((K // 128, R), dtype=torch.int32, device=DEV)
+    fb.fp8bs_mx_quant_1x32(xd, q, sf)
+    assert fb.fp8bs_sync_status() == fb.FP8BS_OK
+    rng = np.random.default_rng(4096)
+    for b in [0, R // 128 - 1] + [int(v) for v in rng.integers(1, R // 128 - 1, 4)]:
+        r0, r1 = 128 * b, 128 * (b + 1)
+        qr, sfr = oracle.mx_quant_1x32(oracle_input(x[r0:r1]))
+        assert np.array_equal(q[r0:r1].cpu().numpy(), qr), f"codes, block {b}"
+        w = np.ascontiguousarray(sf[:, r0:r1].cpu().numpy())
+        assert np.array_equal(w.view(np.uint8).reshape(K // 128, 128, 4), sfr), f"exponents, block {b}"

@@ -5,9 +5,10 @@ import numpy as np
 import pytest
 import torch
 
+import fp8_fine_grained_15_b300 as fb
 import oracle
 import workloads as wl
-from gpu_helpers import (gpu_quant_1x128, gpu_quant_128x1, gpu_quant_dual, gpu_quant_w,
+from gpu_helpers import (DEV, gpu_quant_1x128, gpu_quant_128x1, gpu_quant_dual, gpu_quant_w,
                          oracle_input)
 
 pytestmark = pytest.mark.gpu
@@ -204,3 +205,30 @@ def test_quant_dual_layer_activations_and_grads():
     """The layer step's two activation tensors, in full."""
     _check_dual(wl.layer_activations(), "X 4096x7168")
     _check_dual(wl.layer_grad_output(), "dY 4096x18432")
+
+
+def test_dual_quantizer_at_sweep_maximum_sampled():
+    """The sweep's largest case, 65536 x 7168 bf16 (56 x 512 CTAs), through the
+    dual quantizer; token blocks are independent, so whole 128-token blocks
+    (first, last and random ones) are compared bit-exactly with the oracle."""
+    x = wl.sweep_activations(65536)
+    T, C = x.shape
+    xd = x.to(DEV)
+    dev = xd.device
+    q = torch.empty((T, C), dtype=torch.uint8, device=dev)
+    s = torch.empty((C // 128, T), dtype=torch.float32, device=dev)
+    qT = torch.empty((C, T), dtype=torch.uint8, device=dev)
+    sT = torch.empty((T // 128, C), dtype=torch.float32, device=dev)
+    fb.fp8bs_quant_act_dual(xd, q, s, qT, sT)
+    assert fb.fp8bs_sync_status() == fb.FP8BS_OK
+    rng = np.random.default_rng(65536)
+    blocks = [0, T // 128 - 1] + [int(b) for b in rng.integers(1, T // 128 - 1, 4)]
+    for b in blocks:
+        r0, r1 = 128 * b, 128 * (b + 1)
+        xb = oracle_input(x[r0:r1])
+        qr, sr = oracle.quant_act_1x128(xb)
+        qTr, sTr = oracle.quant_act_128x1(xb)
+        _eq(q[r0:r1].cpu().numpy(), qr, f"1x128 codes, block {b}")
+        _eq(s[:, r0:r1].cpu().numpy(), sr, f"1x128 scales, block {b}")
+        _eq(qT[:, r0:r1].cpu().numpy(), qTr, f"128x1 codes, block {b}")
+        _eq(sT[b:b + 1].cpu().numpy(), sTr, f"128x1 scales, block {b}")
