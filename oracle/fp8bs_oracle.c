@@ -21,7 +21,7 @@
  *  - untitled page at jp-study.kr, Figure 7 (b) passage: partial sums are
  *    promoted to FP32 on CUDA cores, where the scales are applied.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *  - E4M3 is the OCP "E4M3FN" layout: bias 7, no infinities, S.1111.111 = NaN,
  *    largest finite 448.  Encoding rounds to nearest, ties to even, and
  *    saturates finite overflow to +-448 ("satfinite").  The sign of zero is
@@ -306,7 +306,7 @@ void fp8bs_oracle_gemm_elements(int64_t K,
  * to microscaling formats, with group scaling done by the tensor cores of the
  * next GPU generation, as the direction fine-grained quantization takes.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *  - Groups are 1x32 along the contraction axis for both operands.  A group's
  *    scale is a power of two 2^e stored as an unsigned 8-bit exponent
  *    (UE8M0: byte = e + 127, e in [-127, 127]).
