@@ -58,7 +58,7 @@ def dual_bytes(elems: int, in_bytes: int) -> float:
 # the sha256 of the kernel source it was measured on; ignored once the source changes.
 NCU_TRAFFIC = {
     # ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch of
-    # `bench.py --case wgrad` (profiles/gemm_pair_layer_ncu_full.md)
+    # `bench.py --case wgrad`, measured by ncu on that one launch
     "gemm_wgrad": {"file": "gemm_pair_kernel.cuh", "src": "04c1dbfdadbd7d84",
                    "bytes": 191641344 + 496067328},
 }

@@ -675,9 +675,15 @@ fp8bs_status fp8bs_gemm_static_ws(int64_t M, int64_t N, int64_t K, const uint8_t
                                   int64_t lda, const float* sa, int64_t ldsa, const uint8_t* B,
                                   int64_t ldb, const float* sb, fp8bs_bscale sb_mode, int64_t ldsb,
                                   void* C, fp8bs_dtype ct, int64_t ldc, void* stream) {
+  // The argument checks of fp8bs_gemm_ws come first, on the host, so a bad
+  // call returns the same status and touches no device state.
+  fp8bs_status st = check_gemm(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc);
+  if (st != FP8BS_OK || M == 0 || N == 0) return st;
+  if (K == 0)   // nothing to split: the contraction is empty and C is zero-filled
+    return gemm_dense(M, N, K, A, lda, sa, ldsa, B, ldb, sb, sb_mode, ldsb, C, ct, ldc, nullptr, 0,
+                      stream);
   size_t need = 0;
-  fp8bs_status st = fp8bs_gemm_workspace_size(M, N, K, &need);
-  if (st != FP8BS_OK) return st;
+  if ((st = fp8bs_gemm_workspace_size(M, N, K, &need)) != FP8BS_OK) return st;
   if (need > kStaticWsBytes) return FP8BS_ERR_UNSUPPORTED;   // more scratch than the array holds
   void* ws = nullptr;
   if ((st = static_workspace(&ws)) != FP8BS_OK) return st;

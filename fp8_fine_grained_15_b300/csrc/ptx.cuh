@@ -1,10 +1,14 @@
 // Thin inline-PTX wrappers for sm_103a: mbarrier (with bounded waits), TMA tile
 // loads, and the tcgen05 family (TMEM alloc, MMA, commit, load, fences).
 //
-// Every wait in this library goes through bounded_wait(): it gives up after
-// kSpinLimitNs nanoseconds of %globaltimer, records FP8BS_DEVERR_TIMEOUT in the
-// device error word and raises the CTA's abort flag, so a protocol mistake ends
-// the kernel with an error status instead of a hung GPU.
+// Every wait in this library is bounded.  The hot-path waits (bounded_wait)
+// count SM clock cycles with clock64 and give up after kSpinLimitCycles; the
+// waits while a kernel drains its own copies (bounded_wait_noabort) count
+// nanoseconds of %globaltimer.  Both limits come from FP8BS_SPIN_LIMIT_NS
+// (cycles at the 2032 MHz maximum SM clock, so a hot-path wait lasts longer in
+// wall time when the clock is lower).  On expiry the kernel records a timeout
+// in the device error word and raises the CTA's abort flag, so a protocol
+// mistake ends the kernel with an error status instead of a hung GPU.
 #pragma once
 #include <cstdint>
 
@@ -19,9 +23,10 @@ __device__ uint32_t g_device_error = 0;
 #define FP8BS_SPIN_LIMIT_NS (1ull << 30)   // ~1.07 s: far above any legal wait
 #endif
 constexpr uint64_t kSpinLimitNs = FP8BS_SPIN_LIMIT_NS;
-// The same limit for the hot-path waits, in SM cycles: 2^31 cycles is ~1.06 s
-// at the 2032 MHz maximum clock (longer at lower clocks).
-constexpr long long kSpinLimitCycles = 1ll << 31;
+// The same limit for the hot-path waits, in SM cycles at the 2032 MHz maximum
+// clock (2^30 ns -> ~2.2e9 cycles; at lower clocks the wait lasts longer).
+constexpr long long kSpinLimitCycles = static_cast<long long>(kSpinLimitNs / 1000ull * 2032ull);
+static_assert(kSpinLimitCycles > 0, "FP8BS_SPIN_LIMIT_NS must be at least 1 us");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -126,21 +131,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void* tmap,
       " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst_smem),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
       "l"(policy)
-      : "memory");
-}
-
-// Same, multicast: the box lands at the same shared-memory offset in every CTA
-// of cta_mask and signals the mbarrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst_smem, const void* tmap,
-                                                      int32_t c0, int32_t c1, int32_t c2,
-                                                      uint64_t* bar, uint16_t cta_mask,
-                                                      uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6, %7;" ::"r"(dst_smem),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
-      "h"(cta_mask), "l"(policy)
       : "memory");
 }
 
@@ -270,15 +260,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// Same, arriving on the barrier at the same offset in every CTA of cta_mask.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 

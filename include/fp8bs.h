@@ -231,7 +231,10 @@ fp8bs_status fp8bs_gemm_accumulate(int64_t M, int64_t N, int64_t K,
  * the library's own device memory, which every GPU that loads the library
  * holds until the process exits.  The paper has no counterpart of this call.
  *   Arguments, requirements and results are those of fp8bs_gemm_ws with a
- *   20 MiB workspace (the split is chosen the same way).
+ *   20 MiB workspace (the split is chosen the same way, so the two give
+ *   bit-identical outputs).  The arguments are checked on the host first, as
+ *   fp8bs_gemm_ws checks them: a bad call returns the same status and touches
+ *   no device state.
  *   A shape whose fp8bs_gemm_workspace_size exceeds 20 MiB is rejected with
  *   FP8BS_ERR_UNSUPPORTED before any launch (on a 148-SM B300 no shape needs
  *   more than 74 partial tiles, 18.5 MiB).

@@ -139,6 +139,27 @@ def test_gemm_ws_host_checks(L):
                            fb.FP8BS_SB_BLOCK_KN, 2, NULL, BF16, 256, NULL, 0, None) == fb.FP8BS_OK
 
 
+@pytest.mark.parametrize("kw", [
+    dict(K=100), dict(N=200), dict(mode=9), dict(A=NULL), dict(lda=128), dict(ldsa=64),
+    dict(ldsb=1), dict(lda=264), dict(B=FAKE_ODD), dict(ldc=260), dict(M=-1), dict(C=NULL),
+    dict(ct=7), dict(M=0),
+])
+def test_static_ws_rejects_like_gemm_ws(L, kw):
+    """The no-allocation GEMM checks its arguments on the host before anything
+    else, so a bad call returns what fp8bs_gemm_ws returns for it (and never
+    reaches the device: these pointers are fake)."""
+    a = dict(M=128, N=256, K=256, A=FAKE, lda=256, sa=FAKE, ldsa=128, B=FAKE, ldb=256, sb=FAKE,
+             mode=fb.FP8BS_SB_BLOCK_KN, ldsb=2, C=FAKE, ct=BF16, ldc=256)
+    a.update(kw)
+    args = (a["M"], a["N"], a["K"], a["A"], a["lda"], a["sa"], a["ldsa"], a["B"], a["ldb"],
+            a["sb"], a["mode"], a["ldsb"], a["C"], a["ct"], a["ldc"])
+    want = L.fp8bs_gemm_ws(*args, NULL, 0, None)
+    got = L.fp8bs_gemm_static_ws(*args, None)
+    assert got == want
+    if a["M"] != 0:
+        assert got != fb.FP8BS_OK
+
+
 def test_dispatch_host_checks(L):
     args = lambda E, M_cap, K=128, T=100: (FAKE, BF16, T, K, K, FAKE, E, FAKE, K, FAKE, M_cap,  # noqa: E731
                                           M_cap, FAKE, FAKE, FAKE, FAKE, None)

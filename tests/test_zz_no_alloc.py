@@ -1,21 +1,28 @@
 """fp8bs_gemm_static_ws, the GEMM entry point for callers that cannot
 allocate device memory (they cannot call cudaMalloc where they run, or have
 no workspace to lend): its split-K partials live in the library's own device
-array instead of a caller workspace.  Called through the C ABI twice in a
-row, it must give what fp8bs_gemm_ws with a caller workspace gives, within
-the GEMM tolerance of the other tests (and both must meet it against the CPU
-oracle).  This file is collected last so that a run stopping at its first
-failure has already run every other test; it also passes alone."""
+array instead of a caller workspace.
+
+Called through the C ABI twice in a row, it must give exactly what
+fp8bs_gemm_ws gives with a caller workspace (the two choose the same split,
+so the outputs are bit-identical), and both must meet the GEMM tolerance of
+the other tests against the CPU oracle.  Between the two calls an unrelated
+split shape runs through the same array, so the second call can only match
+if it rewrites every partial it reads.  This file is collected last so that
+a run stopping at its first failure has already run every other test; it also
+passes alone in a fresh process."""
 import numpy as np
 import pytest
 import torch
 
 import fp8_fine_grained_15_b300 as fb
 import oracle
-from gpu_helpers import (DEV, MODES, assert_gemm_close, gemm_bound, gemm_operands, gpu_gemm_ws,
-                         to_dev_f32, to_dev_u8)
+from gpu_helpers import (DEV, MODES, assert_gemm_close, gemm_operands, gpu_gemm_ws, to_dev_f32,
+                         to_dev_u8)
 
 pytestmark = pytest.mark.gpu
+
+STATIC_BYTES = 20 << 20
 
 
 def _static_ws_call(Aq, sa, Bq, sb, mode, out_dtype):
@@ -33,20 +40,29 @@ def _static_ws_call(Aq, sa, Bq, sb, mode, out_dtype):
     return C.float().cpu().numpy().astype(np.float64)
 
 
-@pytest.mark.parametrize("M,N,K,mode,out", [
-    (512, 1024, 2048, "NK", torch.float32),     # 8 tiles, each split in 8 K-ranges
-    (256, 512, 4096, "KN", torch.bfloat16),     # 2 tiles, 32 K-ranges each
+@pytest.mark.parametrize("M,N,K,mode,out,other", [
+    # 8 tiles, each split in 8 K-ranges; in between, 2 tiles x 32 ranges
+    (512, 1024, 2048, "NK", torch.float32, (256, 512, 4096, "KN", torch.bfloat16)),
+    # 2 tiles, 32 K-ranges each; in between, a ragged per-column shape
+    (256, 512, 4096, "KN", torch.bfloat16, (300, 272, 2048, "PERCOL", torch.float32)),
 ])
-def test_static_workspace_gemm_matches_workspace_gemm(M, N, K, mode, out):
+def test_static_workspace_gemm_matches_workspace_gemm(M, N, K, mode, out, other):
     need = fb.fp8bs_gemm_workspace_size(M, N, K)
-    assert 0 < need <= 20 << 20          # the shape splits and fits the static array
+    assert 0 < need <= STATIC_BYTES          # the shape splits and fits the static array
     Aq, sa, Bq, sb = gemm_operands(M, N, K, mode, seed=M + N + 3 * K)
     c_ws = gpu_gemm_ws(Aq, sa, Bq, sb, MODES[mode], out_dtype=out)
     c_ref, s_abs = oracle.gemm(Aq, sa, Bq, sb, MODES[mode])
     bf16 = out == torch.bfloat16
     assert_gemm_close(c_ws, c_ref, s_abs, bf16, "caller workspace")
-    bound = gemm_bound(c_ref, s_abs, bf16)
-    for call in range(2):                # the array keeps the previous call's partials
+
+    oM, oN, oK, omode, oout = other
+    assert fb.fp8bs_gemm_workspace_size(oM, oN, oK) > 0
+    oAq, osa, oBq, osb = gemm_operands(oM, oN, oK, omode, seed=oM + oN + oK)
+    for call in range(2):
         c = _static_ws_call(Aq, sa, Bq, sb, mode, out)
-        assert np.all(np.abs(c - c_ws) <= bound), f"call {call}: differs from fp8bs_gemm_ws"
+        assert np.array_equal(c, c_ws), f"call {call}: differs from fp8bs_gemm_ws"
         assert_gemm_close(c, c_ref, s_abs, bf16, f"static workspace, call {call}")
+        if call == 0:   # leave unrelated partials in the array before the second call
+            c_other = _static_ws_call(oAq, osa, oBq, osb, omode, oout)
+            o_ref, o_abs = oracle.gemm(oAq, osa, oBq, osb, MODES[omode])
+            assert_gemm_close(c_other, o_ref, o_abs, oout == torch.bfloat16, "interleaved shape")
