@@ -8,7 +8,13 @@ The arithmetic lives in ``fp8bs_oracle.c`` (plain C, binary32 quantization,
 binary64 GEMM); this module compiles it with gcc on first use and wraps it with
 numpy arrays.  Grouped GEMM is the dense oracle applied expert by expert.
 The MX variant (UE8M0 power-of-two scales on 1x32 groups, applied per group)
-has its own quantizer and GEMM in the same file.
+has its own quantizer and GEMM in the same file, and so does the
+quantize-then-dispatch step of MoE layers (stable grouping of tokens by
+expert, padding to 128 rows, 1x128 quantization of each routed row).
+
+The GEMMs split their output elements over POSIX threads (one per online CPU
+unless ``set_threads`` says otherwise); each element is computed by the same
+loop in the same order whatever the thread count.
 
 Every function cites the passage it restates in the C source's header.  Pins
 (tests/test_oracle_pins.py) tie it to the OCP E4M3 format, to PyTorch's own
@@ -38,7 +44,7 @@ def build(force: bool = False) -> str:
         tmp = _LIB + f".{os.getpid()}.tmp"
         subprocess.check_call(
             ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-             "-fno-fast-math", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
+             "-fno-fast-math", "-Wall", "-Wextra", "-pthread", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -68,6 +74,13 @@ def _load():
         for f in ("quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm",
                   "gemm_elements", "mx_quant_1x32", "mx_gemm", "mx_gemm_elements"):
             getattr(lib, "fp8bs_oracle_" + f).restype = None
+        lib.fp8bs_oracle_set_threads.argtypes = [I]
+        lib.fp8bs_oracle_set_threads.restype = None
+        lib.fp8bs_oracle_threads.argtypes = []
+        lib.fp8bs_oracle_threads.restype = I
+        lib.fp8bs_oracle_dispatch.argtypes = [P, I, I64, I64, I64, P, ctypes.c_int32, I64, P, I64,
+                                              P, I64, P, P, P, P]
+        lib.fp8bs_oracle_dispatch.restype = I64
         _lib = lib
     return _lib
 
@@ -84,6 +97,16 @@ def _as_input(x: np.ndarray):
     if x.dtype == np.uint16:
         return x, BF16
     raise TypeError(f"oracle input must be float32 or bf16 bits (uint16), got {x.dtype}")
+
+
+def set_threads(n: int) -> None:
+    """Threads the GEMMs use (n <= 0: one per online CPU)."""
+    _load().fp8bs_oracle_set_threads(int(n))
+
+
+def threads() -> int:
+    """Threads the GEMMs use now."""
+    return int(_load().fp8bs_oracle_threads())
 
 
 # ------------------------------------------------------------------ E4M3
@@ -294,3 +317,34 @@ def mx_gemm_elements(A, sfa, B, sfb, rows, cols):
     _load().fp8bs_oracle_mx_gemm_elements(K, _ptr(A), K, _ptr(sfa), M, _ptr(B), K, _ptr(sfb), N,
                                           rows.size, _ptr(rows), _ptr(cols), _ptr(c), _ptr(a))
     return c, a
+
+
+# ------------------------------------------------- quantize-then-dispatch
+
+def dispatch(x: np.ndarray, expert: np.ndarray, E: int):
+    """Quantize-then-dispatch by its steps (see the C source): tokens grouped
+    by expert in token order, each expert padded to a multiple of 128 rows,
+    routed rows quantized 1x128, padding rows codes 0 / scale 1.  x [T x K]
+    (float32 or bf16 bits), expert [T] ints (ids outside [0, E) are dropped).
+    Returns (q [n x K], s [K/128 x n], offsets [E+1], counts [E],
+    token_row [T] (-1 for dropped tokens), row_token [n] (-1 on padding rows),
+    dropped), n = offsets[E]."""
+    x, dt = _as_input(x)
+    T, K = x.shape
+    assert K % 128 == 0
+    expert = np.ascontiguousarray(expert, np.int32)
+    assert expert.shape == (T,)
+    M_cap = (T + 127 * E + 127) // 128 * 128
+    q = np.zeros((max(M_cap, 1), K), np.uint8)
+    s = np.zeros((K // 128, max(M_cap, 1)), np.float32)
+    offsets = np.zeros(E + 1, np.int64)
+    counts = np.zeros(E, np.int64)
+    token_row = np.zeros(max(T, 1), np.int64)
+    row_token = np.zeros(max(M_cap, 1), np.int64)
+    dropped = _load().fp8bs_oracle_dispatch(
+        _ptr(x), dt, T, K, K, _ptr(expert), E, M_cap, _ptr(q), K, _ptr(s), s.shape[1],
+        _ptr(offsets), _ptr(counts), _ptr(token_row), _ptr(row_token))
+    assert dropped >= 0
+    n = int(offsets[E])
+    return (q[:n], np.ascontiguousarray(s[:, :n]), offsets, counts, token_row[:T],
+            row_token[:n], int(dropped))

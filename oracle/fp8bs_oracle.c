@@ -40,10 +40,19 @@
  * with -ffp-contract=off, no fast-math).  The GEMM accumulates in binary64; the
  * inner 128-term sum of decoded-code products is exact in binary64 (each
  * product has at most 8 significant bits and exponents within [-18, 18]).
+ *
+ * Threads: the quantizers hand whole tiles, the GEMMs whole output rows (or,
+ * for the element lists, whole elements) to POSIX threads.  Every tile and
+ * every element is still computed by the same loop, in the same order, by one
+ * thread, so the results do not depend on the thread count; threads only split
+ * the list of independent pieces.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
+#include <unistd.h>
 
 /* ------------------------------------------------------------------ E4M3 */
 
@@ -149,26 +158,131 @@ static uint8_t quantize_value(float x, float r)
     return fp8bs_oracle_e4m3_encode(y);
 }
 
+/* --------------------------------------------------------------- threads */
+
+static int g_threads = 0;          /* 0: one per online CPU */
+
+/* Number of threads the quantizers and GEMMs use (n <= 0: one per online CPU). */
+void fp8bs_oracle_set_threads(int n)
+{
+    g_threads = n > 0 ? n : 0;
+}
+
+int fp8bs_oracle_threads(void)
+{
+    long n = g_threads > 0 ? g_threads : sysconf(_SC_NPROCESSORS_ONLN);
+    if (n < 1)
+        n = 1;
+    if (n > 256)
+        n = 256;
+    return (int)n;
+}
+
+/* Run body(ctx, t, nt) on nt threads, t = 0 .. nt-1; thread t takes items
+ * t, t + nt, t + 2 nt, ... of whatever list the body walks. */
+struct thread_arg {
+    void (*body)(void *, int, int);
+    void *ctx;
+    int t, nt;
+};
+
+static void *thread_main(void *p)
+{
+    struct thread_arg *a = (struct thread_arg *)p;
+    a->body(a->ctx, a->t, a->nt);
+    return NULL;
+}
+
+static void run_threads(void (*body)(void *, int, int), void *ctx, int64_t items)
+{
+    int nt = fp8bs_oracle_threads(), t, started = 0;
+    pthread_t tid[256];
+    struct thread_arg args[256];
+    if (items < nt)
+        nt = items > 0 ? (int)items : 1;
+    for (t = 0; t < nt; ++t) {
+        args[t].body = body;
+        args[t].ctx = ctx;
+        args[t].t = t;
+        args[t].nt = nt;
+    }
+    for (t = 1; t < nt; ++t) {
+        if (pthread_create(&tid[t], NULL, thread_main, &args[t]) != 0)
+            break;
+        started = t;
+    }
+    /* items of threads that could not be started run here, in this thread */
+    for (t = started + 1; t < nt; ++t)
+        body(ctx, t, nt);
+    body(ctx, 0, nt);
+    for (t = 1; t <= started; ++t)
+        pthread_join(tid[t], NULL);
+}
+
 /* ----------------------------------------------------------- quantizers */
+
+/* Arguments of one quantizer call, shared by its threads; every tile is
+ * quantized whole by one thread, so the result does not depend on how many
+ * threads there are. */
+struct quant_job {
+    const void *x;
+    int dtype;
+    int64_t rows, cols, ldx;
+    uint8_t *q;
+    int64_t ldq;
+    uint8_t *qT;
+    int64_t ldqT;
+    float *s;
+    int64_t lds;
+};
+
+/* 1x128 tiles of rows m = t, t + nt, ... */
+static void quant_1x128_rows(void *p, int t, int nt)
+{
+    const struct quant_job *j = (const struct quant_job *)p;
+    for (int64_t m = t; m < j->rows; m += nt) {
+        for (int64_t kb = 0; kb < j->cols / 128; ++kb) {
+            float amax = 0.0f, sc, r;
+            for (int c = 0; c < 128; ++c) {
+                float a = fabsf(load_elem(j->x, j->dtype, j->ldx, m, kb * 128 + c));
+                if (a > amax)
+                    amax = a;
+            }
+            tile_scale(amax, &sc, &r);
+            for (int c = 0; c < 128; ++c)
+                j->q[m * j->ldq + kb * 128 + c] =
+                    quantize_value(load_elem(j->x, j->dtype, j->ldx, m, kb * 128 + c), r);
+            j->s[kb * j->lds + m] = sc;
+        }
+    }
+}
 
 /* 1x128 activation tiles: x [M x K] row-major (leading dim ldx elements).
  * q [M x K] (ldq bytes per row); s [K/128][lds] with s[kb*lds + m]. */
 void fp8bs_oracle_quant_act_1x128(const void *x, int dtype, int64_t M, int64_t K, int64_t ldx,
                                   uint8_t *q, int64_t ldq, float *s, int64_t lds)
 {
-    for (int64_t m = 0; m < M; ++m) {
-        for (int64_t kb = 0; kb < K / 128; ++kb) {
+    struct quant_job j = {x, dtype, M, K, ldx, q, ldq, NULL, 0, s, lds};
+    run_threads(quant_1x128_rows, &j, M);
+}
+
+/* 128x1 tiles of token blocks tb = t, t + nt, ... (all channels). */
+static void quant_128x1_blocks(void *p, int t, int nt)
+{
+    const struct quant_job *j = (const struct quant_job *)p;
+    for (int64_t tb = t; tb < j->rows / 128; tb += nt) {
+        for (int64_t c = 0; c < j->cols; ++c) {
             float amax = 0.0f, sc, r;
-            for (int c = 0; c < 128; ++c) {
-                float a = fabsf(load_elem(x, dtype, ldx, m, kb * 128 + c));
+            for (int i = 0; i < 128; ++i) {
+                float a = fabsf(load_elem(j->x, j->dtype, j->ldx, tb * 128 + i, c));
                 if (a > amax)
                     amax = a;
             }
             tile_scale(amax, &sc, &r);
-            for (int c = 0; c < 128; ++c)
-                q[m * ldq + kb * 128 + c] =
-                    quantize_value(load_elem(x, dtype, ldx, m, kb * 128 + c), r);
-            s[kb * lds + m] = sc;
+            for (int i = 0; i < 128; ++i)
+                j->qT[c * j->ldqT + tb * 128 + i] =
+                    quantize_value(load_elem(j->x, j->dtype, j->ldx, tb * 128 + i, c), r);
+            j->s[tb * j->lds + c] = sc;
         }
     }
 }
@@ -179,19 +293,34 @@ void fp8bs_oracle_quant_act_1x128(const void *x, int dtype, int64_t M, int64_t K
 void fp8bs_oracle_quant_act_128x1(const void *x, int dtype, int64_t T, int64_t C, int64_t ldx,
                                   uint8_t *qT, int64_t ldq, float *s, int64_t lds)
 {
-    for (int64_t tb = 0; tb < T / 128; ++tb) {
-        for (int64_t c = 0; c < C; ++c) {
+    struct quant_job j = {x, dtype, T, C, ldx, NULL, 0, qT, ldq, s, lds};
+    run_threads(quant_128x1_blocks, &j, T / 128);
+}
+
+/* 128x128 blocks of block rows rb = t, t + nt, ... */
+static void quant_128x128_blockrows(void *p, int t, int nt)
+{
+    const struct quant_job *j = (const struct quant_job *)p;
+    const int64_t C = j->cols;
+    for (int64_t rb = t; rb < j->rows / 128; rb += nt) {
+        for (int64_t cb = 0; cb < C / 128; ++cb) {
             float amax = 0.0f, sc, r;
-            for (int t = 0; t < 128; ++t) {
-                float a = fabsf(load_elem(x, dtype, ldx, tb * 128 + t, c));
-                if (a > amax)
-                    amax = a;
-            }
+            for (int i = 0; i < 128; ++i)
+                for (int k = 0; k < 128; ++k) {
+                    float a = fabsf(load_elem(j->x, j->dtype, j->ldx, rb * 128 + i, cb * 128 + k));
+                    if (a > amax)
+                        amax = a;
+                }
             tile_scale(amax, &sc, &r);
-            for (int t = 0; t < 128; ++t)
-                qT[c * ldq + tb * 128 + t] =
-                    quantize_value(load_elem(x, dtype, ldx, tb * 128 + t, c), r);
-            s[tb * lds + c] = sc;
+            for (int i = 0; i < 128; ++i)
+                for (int k = 0; k < 128; ++k) {
+                    int64_t row = rb * 128 + i, col = cb * 128 + k;
+                    uint8_t code = quantize_value(load_elem(j->x, j->dtype, j->ldx, row, col), r);
+                    j->q[row * j->ldq + col] = code;
+                    if (j->qT)
+                        j->qT[col * j->ldqT + row] = code;
+                }
+            j->s[rb * (C / 128) + cb] = sc;
         }
     }
 }
@@ -201,27 +330,8 @@ void fp8bs_oracle_quant_act_128x1(const void *x, int dtype, int64_t T, int64_t C
 void fp8bs_oracle_quant_w_128x128(const void *w, int dtype, int64_t R, int64_t C, int64_t ldw,
                                   uint8_t *q, int64_t ldq, uint8_t *qT, int64_t ldqT, float *s)
 {
-    for (int64_t rb = 0; rb < R / 128; ++rb) {
-        for (int64_t cb = 0; cb < C / 128; ++cb) {
-            float amax = 0.0f, sc, r;
-            for (int i = 0; i < 128; ++i)
-                for (int j = 0; j < 128; ++j) {
-                    float a = fabsf(load_elem(w, dtype, ldw, rb * 128 + i, cb * 128 + j));
-                    if (a > amax)
-                        amax = a;
-                }
-            tile_scale(amax, &sc, &r);
-            for (int i = 0; i < 128; ++i)
-                for (int j = 0; j < 128; ++j) {
-                    int64_t row = rb * 128 + i, col = cb * 128 + j;
-                    uint8_t code = quantize_value(load_elem(w, dtype, ldw, row, col), r);
-                    q[row * ldq + col] = code;
-                    if (qT)
-                        qT[col * ldqT + row] = code;
-                }
-            s[rb * (C / 128) + cb] = sc;
-        }
-    }
+    struct quant_job j = {w, dtype, R, C, ldw, q, ldq, qT, ldqT, s, 0};
+    run_threads(quant_128x128_blockrows, &j, R / 128);
 }
 
 /* ----------------------------------------------------------------- GEMM */
@@ -271,18 +381,51 @@ static void decode_table(double dec[256])
         dec[v] = fp8bs_oracle_e4m3_decode((uint8_t)v);
 }
 
+struct gemm_job {
+    int64_t M, N, K;
+    const uint8_t *A;
+    int64_t lda;
+    const float *sa;
+    int64_t ldsa;
+    const uint8_t *B;
+    int64_t ldb;
+    const float *sb;
+    int mode;
+    int64_t ldsb;
+    const int64_t *rows, *cols;    /* element lists (NULL: whole rows) */
+    double *c_ref, *s_abs;
+    double dec[256];
+};
+
+/* Rows t, t + nt, ... of the full output. */
+static void gemm_rows(void *p, int t, int nt)
+{
+    const struct gemm_job *g = (const struct gemm_job *)p;
+    for (int64_t i = t; i < g->M; i += nt)
+        for (int64_t j = 0; j < g->N; ++j)
+            gemm_one(g->K, g->A, g->lda, g->sa, g->ldsa, g->B, g->ldb, g->sb, g->mode, g->ldsb,
+                     g->dec, i, j, &g->c_ref[i * g->N + j], &g->s_abs[i * g->N + j]);
+}
+
+/* Elements t, t + nt, ... of the list. */
+static void gemm_list(void *p, int t, int nt)
+{
+    const struct gemm_job *g = (const struct gemm_job *)p;
+    for (int64_t e = t; e < g->M; e += nt)
+        gemm_one(g->K, g->A, g->lda, g->sa, g->ldsa, g->B, g->ldb, g->sb, g->mode, g->ldsb,
+                 g->dec, g->rows[e], g->cols[e], &g->c_ref[e], &g->s_abs[e]);
+}
+
 /* Full M x N output into c_ref / s_abs (row-major, N per row). */
 void fp8bs_oracle_gemm(int64_t M, int64_t N, int64_t K,
                        const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa,
                        const uint8_t *B, int64_t ldb, const float *sb, int mode, int64_t ldsb,
                        double *c_ref, double *s_abs)
 {
-    double dec[256];
-    decode_table(dec);
-    for (int64_t i = 0; i < M; ++i)
-        for (int64_t j = 0; j < N; ++j)
-            gemm_one(K, A, lda, sa, ldsa, B, ldb, sb, mode, ldsb, dec, i, j,
-                     &c_ref[i * N + j], &s_abs[i * N + j]);
+    struct gemm_job g = {M, N, K, A, lda, sa, ldsa, B, ldb, sb, mode, ldsb,
+                         NULL, NULL, c_ref, s_abs, {0}};
+    decode_table(g.dec);
+    run_threads(gemm_rows, &g, M);
 }
 
 /* Selected output elements (rows[e], cols[e]) for e < count. */
@@ -292,11 +435,10 @@ void fp8bs_oracle_gemm_elements(int64_t K,
                                 int64_t count, const int64_t *rows, const int64_t *cols,
                                 double *c_ref, double *s_abs)
 {
-    double dec[256];
-    decode_table(dec);
-    for (int64_t e = 0; e < count; ++e)
-        gemm_one(K, A, lda, sa, ldsa, B, ldb, sb, mode, ldsb, dec, rows[e], cols[e],
-                 &c_ref[e], &s_abs[e]);
+    struct gemm_job g = {count, 0, K, A, lda, sa, ldsa, B, ldb, sb, mode, ldsb,
+                         rows, cols, c_ref, s_abs, {0}};
+    decode_table(g.dec);
+    run_threads(gemm_list, &g, count);
 }
 
 /* ------------------------------------------------- MX (microscaling) variant
@@ -391,17 +533,47 @@ static void mx_gemm_one(int64_t K, const uint8_t *A, int64_t lda, const uint8_t 
     *abs_out = sabs;
 }
 
+struct mx_job {
+    int64_t M, N, K;
+    const uint8_t *A;
+    int64_t lda;
+    const uint8_t *sfa;
+    int64_t ldsfa;
+    const uint8_t *B;
+    int64_t ldb;
+    const uint8_t *sfb;
+    int64_t ldsfb;
+    const int64_t *rows, *cols;    /* element lists (NULL: whole rows) */
+    double *c_ref, *s_abs;
+    double dec[256];
+};
+
+static void mx_rows(void *p, int t, int nt)
+{
+    const struct mx_job *g = (const struct mx_job *)p;
+    for (int64_t i = t; i < g->M; i += nt)
+        for (int64_t j = 0; j < g->N; ++j)
+            mx_gemm_one(g->K, g->A, g->lda, g->sfa, g->ldsfa, g->B, g->ldb, g->sfb, g->ldsfb,
+                        g->dec, i, j, &g->c_ref[i * g->N + j], &g->s_abs[i * g->N + j]);
+}
+
+static void mx_list(void *p, int t, int nt)
+{
+    const struct mx_job *g = (const struct mx_job *)p;
+    for (int64_t e = t; e < g->M; e += nt)
+        mx_gemm_one(g->K, g->A, g->lda, g->sfa, g->ldsfa, g->B, g->ldb, g->sfb, g->ldsfb,
+                    g->dec, g->rows[e], g->cols[e], &g->c_ref[e], &g->s_abs[e]);
+}
+
 void fp8bs_oracle_mx_gemm(int64_t M, int64_t N, int64_t K,
                           const uint8_t *A, int64_t lda, const uint8_t *sfa, int64_t ldsfa,
                           const uint8_t *B, int64_t ldb, const uint8_t *sfb, int64_t ldsfb,
                           double *c_ref, double *s_abs)
 {
-    double dec[256];
-    decode_table(dec);
-    for (int64_t i = 0; i < M; ++i)
-        for (int64_t j = 0; j < N; ++j)
-            mx_gemm_one(K, A, lda, sfa, ldsfa, B, ldb, sfb, ldsfb, dec, i, j,
-                        &c_ref[i * N + j], &s_abs[i * N + j]);
+    struct mx_job g = {M, N, K, A, lda, sfa, ldsfa, B, ldb, sfb, ldsfb, NULL, NULL,
+                       c_ref, s_abs, {0}};
+    decode_table(g.dec);
+    run_threads(mx_rows, &g, M);
 }
 
 void fp8bs_oracle_mx_gemm_elements(int64_t K,
@@ -410,9 +582,94 @@ void fp8bs_oracle_mx_gemm_elements(int64_t K,
                                    int64_t count, const int64_t *rows, const int64_t *cols,
                                    double *c_ref, double *s_abs)
 {
-    double dec[256];
-    decode_table(dec);
-    for (int64_t e = 0; e < count; ++e)
-        mx_gemm_one(K, A, lda, sfa, ldsfa, B, ldb, sfb, ldsfb, dec, rows[e], cols[e],
-                    &c_ref[e], &s_abs[e]);
+    struct mx_job g = {count, 0, K, A, lda, sfa, ldsfa, B, ldb, sfb, ldsfb, rows, cols,
+                       c_ref, s_abs, {0}};
+    decode_table(g.dec);
+    run_threads(mx_list, &g, count);
+}
+
+/* ------------------------------------------------ quantize-then-dispatch
+ *
+ * Source: untitled page at jp-study.kr, MoE passage: the activations entering
+ * the MoE up-projection are quantized to FP8 before they are dispatched to
+ * the experts.
+ *
+ * Readings taken where the pages are silent:
+ *  - Tokens are grouped by expert; inside an expert they keep increasing
+ *    token order (a stable grouping, so the row of every token is unique).
+ *  - Every expert's row count is padded up to a multiple of 128 (the 1x128
+ *    tiles of the grouped GEMM never straddle two experts); a padding row is
+ *    a quantized zero row: codes 0, scale 1, and no token.
+ *  - A token whose expert id lies outside [0, E) is dropped (no row).
+ *
+ * Steps, in order:
+ *  1. counts[e] = number of tokens routed to expert e;
+ *  2. offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e] rounded up to 128;
+ *  3. walking the tokens in increasing order, the next free row of the
+ *     token's expert (starting at offsets[e]) becomes token_row[t], and
+ *     row_token[row] = t;
+ *  4. rows offsets[e] + counts[e] .. offsets[e+1] - 1 get row_token -1;
+ *  5. each routed row holds the 1x128 quantization of its token's row of x;
+ *     each padding row holds codes 0 and scale 1.
+ * x [T x K] (ldx elements); q [M_cap x K] (ldq bytes); s[kb*lds + row];
+ * row_token has M_cap entries; rows at or past offsets[E] are not written.
+ * Returns the number of dropped tokens, or -1 if M_cap is too small. */
+int64_t fp8bs_oracle_dispatch(const void *x, int dtype, int64_t T, int64_t K, int64_t ldx,
+                              const int32_t *expert, int32_t E, int64_t M_cap,
+                              uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                              int64_t *offsets, int64_t *counts, int64_t *token_row,
+                              int64_t *row_token)
+{
+    int64_t dropped = 0, *next;
+    const uint16_t *xb = (const uint16_t *)x;
+    const float *xf = (const float *)x;
+
+    for (int32_t e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int64_t t = 0; t < T; ++t)                                    /* step 1 */
+        if (expert[t] >= 0 && expert[t] < E)
+            counts[expert[t]] += 1;
+    offsets[0] = 0;                                                    /* step 2 */
+    for (int32_t e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + (counts[e] + 127) / 128 * 128;
+    if (offsets[E] > M_cap)
+        return -1;
+
+    next = (int64_t *)malloc(sizeof(int64_t) * (size_t)(E > 0 ? E : 1));
+    if (next == NULL)
+        return -1;
+    for (int32_t e = 0; e < E; ++e)
+        next[e] = offsets[e];
+    for (int64_t t = 0; t < T; ++t) {                                  /* step 3 */
+        int32_t e = expert[t];
+        if (e < 0 || e >= E) {
+            token_row[t] = -1;
+            dropped += 1;
+            continue;
+        }
+        token_row[t] = next[e];
+        row_token[next[e]] = t;
+        next[e] += 1;
+    }
+    for (int32_t e = 0; e < E; ++e)                                    /* step 4 */
+        for (int64_t r = offsets[e] + counts[e]; r < offsets[e + 1]; ++r)
+            row_token[r] = -1;
+    free(next);
+
+    for (int64_t r = 0; r < offsets[E]; ++r) {                         /* step 5 */
+        if (row_token[r] < 0) {
+            memset(q + r * ldq, 0, (size_t)K);
+            for (int64_t kb = 0; kb < K / 128; ++kb)
+                s[kb * lds + r] = 1.0f;
+            continue;
+        }
+        /* the one-row 1x128 quantizer applied to row row_token[r] of x */
+        if (dtype == ORACLE_F32)
+            fp8bs_oracle_quant_act_1x128(xf + row_token[r] * ldx, dtype, 1, K, ldx,
+                                         q + r * ldq, ldq, s + r, lds);
+        else
+            fp8bs_oracle_quant_act_1x128(xb + row_token[r] * ldx, dtype, 1, K, ldx,
+                                         q + r * ldq, ldq, s + r, lds);
+    }
+    return dropped;
 }

@@ -1,8 +1,8 @@
-"""Quantize-then-dispatch (fp8bs_quant_dispatch) against the CPU oracle:
-tokens stably sorted by expert, each expert padded to a multiple of 128 rows
-with zero rows, then the oracle's 1x128 quantizer (row-wise, so it commutes
-with the permutation).  Codes, scales, offsets, counts and both row maps must
-match exactly; the dispatched operands then feed the grouped GEMM."""
+"""Quantize-then-dispatch (fp8bs_quant_dispatch) against the CPU oracle's
+dispatch (tokens grouped by expert in token order, each expert padded to a
+multiple of 128 rows with quantized zero rows, routed rows quantized 1x128).
+Codes, scales, offsets, counts and both row maps must match exactly; the
+dispatched operands then feed the grouped GEMM."""
 import numpy as np
 import pytest
 import torch
@@ -16,21 +16,8 @@ pytestmark = pytest.mark.gpu
 
 
 def _oracle_dispatch(x, expert, E):
-    T, K = x.shape
-    counts = np.bincount(expert, minlength=E).astype(np.int64)
-    offsets = np.zeros(E + 1, np.int64)
-    offsets[1:] = np.cumsum((counts + 127) // 128 * 128)
-    order = np.argsort(expert, kind="stable")        # tokens grouped by expert, in token order
-    starts = np.concatenate([[0], np.cumsum(counts)[:-1]])
-    se = expert[order]
-    rows = np.empty(T, np.int64)
-    rows[order] = offsets[se] + (np.arange(T) - starts[se])
-    xp = torch.zeros((int(offsets[E]), K), dtype=x.dtype)
-    xp[torch.from_numpy(rows)] = x
-    row_token = np.full(int(offsets[E]), -1, np.int64)
-    row_token[rows] = np.arange(T)
-    q, s = oracle.quant_act_1x128(oracle_input(xp)) if offsets[E] > 0 else (None, None)
-    return q, s, offsets, counts, rows, row_token
+    q, s, offsets, counts, token_row, row_token, _ = oracle.dispatch(oracle_input(x), expert, E)
+    return q, s, offsets, counts, token_row, row_token
 
 
 def _gpu_dispatch(x, expert, E):
@@ -97,9 +84,13 @@ def test_dispatch_bad_expert_id_reported_and_dropped():
     st, q, s, off, cnt, t2r, r2t = _gpu_dispatch(x, expert, 4)
     assert st == fb.FP8BS_ERR_DEVICE_BAD_ROUTING
     assert t2r[5] == -1
-    keep = np.arange(256) != 5
     assert cnt.sum() == 255
     assert fb.fp8bs_sync_status() == fb.FP8BS_OK   # the error word was cleared
+    qr, sr, offr, cntr, rows, r2tr = _oracle_dispatch(x, expert, 4)   # the token is dropped there too
+    n = int(offr[-1])
+    assert np.array_equal(off, offr) and np.array_equal(cnt, cntr) and np.array_equal(t2r, rows)
+    assert np.array_equal(r2t[:n], r2tr)
+    assert np.array_equal(q[:n], qr) and np.array_equal(s[:, :n], sr)
 
 
 def test_dispatch_then_grouped_gemm():

@@ -318,3 +318,28 @@ def test_grouped_is_dense_per_expert_and_pads_zero():
     rows = np.array([0, 127, 128, 383]); cols = np.array([0, 5, 127, 64])
     ce, _ = oracle.grouped_gemm_elements(offsets, A, sa, B, sb, oracle.SB_BLOCK_KN, rows, cols)
     assert np.array_equal(ce, c[rows, cols])
+
+
+def test_results_do_not_depend_on_the_thread_count():
+    """Threads only split the list of tiles / output elements: one thread and
+    several give bit-identical quantizer and GEMM outputs."""
+    x = random_matrix((384, 640), seed=31, dtype=torch.bfloat16)
+    xb = bf16_bits(x)
+    outs = []
+    try:
+        for nt in (1, 3, 0):
+            oracle.set_threads(nt)
+            q, s = oracle.quant_act_1x128(xb)
+            qT, sT = oracle.quant_act_128x1(xb)
+            wq, wqT, ws = oracle.quant_w_128x128(xb[:384, :512])
+            B, sb = np.ascontiguousarray(qT[:256]), np.ascontiguousarray(sT[:, :256])
+            c, a = oracle.gemm(qT, sT, B, sb, oracle.SB_PERCOL)     # [640 x 256], K = 384
+            rows, cols = np.array([0, 5, 639, 17]), np.array([0, 255, 3, 100])
+            ce, ae = oracle.gemm_elements(qT, sT, B, sb, oracle.SB_PERCOL, rows, cols)
+            assert np.array_equal(ce, c[rows, cols]) and np.array_equal(ae, a[rows, cols])
+            outs.append((q, s, qT, sT, wq, wqT, ws, c, a))
+    finally:
+        oracle.set_threads(0)
+    for other in outs[1:]:
+        for u, v in zip(outs[0], other):
+            assert np.array_equal(u, v)
