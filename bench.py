@@ -43,6 +43,17 @@ METRIC = "block-scaled FP8 GEMM TFLOPS (% of B300 FP8 peak); quantizer GB/s (% o
 WORKLOAD = ("linear-layer training step: quant 1x128/128x1/128x128 + Fprop, Dgrad, Wgrad "
             f"block-scaled FP8 GEMMs, tokens={TOKENS}, K={HIDDEN}, N={FFN}")
 
+DATA = ("synthetic (seeded numpy: N(0,1) activations with 0.1% x100 outliers, "
+        "N(0,0.02) weights, N(0,1e-3) output grads; bf16)")
+
+
+def config_dict(world: int) -> dict:
+    """The workload both arms report (identical in both)."""
+    return {"workload": WORKLOAD, "tokens": TOKENS, "K": HIDDEN, "N": FFN,
+            "l2": "inputs larger than L2 (474 MB of bf16 inputs per step)",
+            "parallelism": f"replicas x{world} (no data-path collective)"}
+
+
 # Algorithmic bytes per element of the quantizers (read input, write codes, write scales).
 def quant_bytes(elems: int, in_bytes: int, transposed_copy: bool = False, block=False) -> float:
     scale = 4.0 / (128 * 128) if block else 4.0 / 128
@@ -281,17 +292,13 @@ def run_fp8bs(args, rank, world, dist_on):
     extras = None if args.no_extras else run_extras(dev, stream, peaks)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(seconds_hint=args.cpu_seconds)
+        cpu = cpu_baseline()
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": "synthetic (seeded numpy: N(0,1) activations with 0.1% x100 outliers, "
-                "N(0,0.02) weights, N(0,1e-3) output grads; bf16)",
-        "config": {"workload": WORKLOAD, "tokens": TOKENS, "K": HIDDEN, "N": FFN,
-                   "l2": "inputs larger than L2 (474 MB of bf16 inputs per step)",
-                   "parallelism": f"replicas x{world} (no data-path collective)"},
+        "data": DATA, "config": config_dict(world),
         "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": step.kernel_launches() * args.steps, "clocks": clk.summary(), "extras": extras,
     }
@@ -491,59 +498,88 @@ def run_extras(dev, stream, peaks):
 
 # ------------------------------------------------------ CPU oracle baseline
 
-CPU_SAMPLE = {"tokens": 256, "K": HIDDEN, "N": 1536}
+# Bounded samples of the layer step for the oracle: the full K and N, fewer
+# tokens (the work per token is the same, so the rate carries over).
+CPU_BASELINE_TOKENS = 512     # one run inside the fp8bs arm: ~10-20 s on 16 cores
+REFERENCE_STEP_TOKENS = 256   # one step of the reference arm
 
 
-def cpu_baseline(seconds_hint: float = 0.0):
-    """The oracle, as it stands (single-threaded C), on a bounded sample of the
-    layer step: the same eight operations on 256 tokens x 7168 x 1536."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+_cpu_inputs_cache: dict = {}
+
+
+def _cpu_inputs(tokens: int):
+    if tokens not in _cpu_inputs_cache:
+        from workloads import bf16_bits
+        _cpu_inputs_cache[tokens] = (bf16_bits(wl.layer_activations(tokens, HIDDEN)),
+                                     bf16_bits(wl.layer_weight(HIDDEN, FFN)),
+                                     bf16_bits(wl.layer_grad_output(tokens, FFN)))
+    return _cpu_inputs_cache[tokens]
+
+
+def cpu_layer_step(tokens: int) -> float:
+    """The oracle, as it stands, on the layer step restricted to `tokens`
+    tokens (same eight operations: dual quantizers as 1x128 + 128x1, the
+    128x128 weight quantizer with its transposed copy, Fprop, Dgrad, Wgrad),
+    on every host core.  Returns the seconds it took."""
     import oracle
-    from workloads import bf16_bits
-    T, K, N = CPU_SAMPLE["tokens"], CPU_SAMPLE["K"], CPU_SAMPLE["N"]
-    x = bf16_bits(wl.layer_activations(T, K))
-    w = bf16_bits(wl.layer_weight(K, N))
-    dy = bf16_bits(wl.layer_grad_output(T, N))
+    x, w, dy = _cpu_inputs(tokens)
     oracle.build()
+    oracle.set_threads(host_cores())
     t0 = time.perf_counter()
     Xq, Sx = oracle.quant_act_1x128(x)
+    XqT, SxT = oracle.quant_act_128x1(x)
     Wq, WqT, Sw = oracle.quant_w_128x128(w)
     oracle.gemm(Xq, Sx, WqT, Sw, oracle.SB_BLOCK_KN)
     dYq, Sdy = oracle.quant_act_1x128(dy)
-    oracle.gemm(dYq, Sdy, Wq, np.ascontiguousarray(Sw.T), oracle.SB_BLOCK_NK)
-    XqT, SxT = oracle.quant_act_128x1(x)
     dYqT, SdyT = oracle.quant_act_128x1(dy)
+    oracle.gemm(dYq, Sdy, Wq, np.ascontiguousarray(Sw.T), oracle.SB_BLOCK_NK)
     oracle.gemm(XqT, SxT, dYqT, SdyT, oracle.SB_PERCOL)
-    dt = time.perf_counter() - t0
-    flops = 3 * 2.0 * T * K * N
-    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOPS", "cores": 1,
-            "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"full layer step (8 ops) on tokens={T}, K={K}, N={N}; "
-                      f"single-threaded C oracle, FP64 GEMM"}
+    return time.perf_counter() - t0
+
+
+def _cpu_sample(tokens: int) -> str:
+    return (f"layer step (8 ops) on tokens={tokens} of {TOKENS}, K={HIDDEN}, N={FFN}; "
+            f"C oracle with FP64 GEMM, one POSIX thread per host core")
+
+
+def cpu_baseline():
+    """The oracle timed on the host cores on a bounded sample of the step."""
+    import oracle
+    T = CPU_BASELINE_TOKENS
+    dt = cpu_layer_step(T)
+    return {"value": round(3 * 2.0 * T * HIDDEN * FFN / dt / 1e12, 6), "unit": "TFLOPS",
+            "cores": oracle.threads(), "kind": "oracle", "seconds": round(dt, 2),
+            "sample": _cpu_sample(T)}
 
 
 def run_reference(args, rank, world, dist_on):
-    """The reference arm: the CPU oracle, timed on the host, on a bounded
-    sample of the same workload, each step one sample."""
+    """The reference arm: the CPU oracle, timed on the host cores, each step
+    one bounded sample of the same workload (the layer step on
+    REFERENCE_STEP_TOKENS tokens); rank 0 only."""
     if rank != 0:
         return None
+    import oracle
+    T = args.ref_tokens
     for _ in range(max(0, min(args.warmup, 1))):
-        cpu_baseline()
-    vals, secs = [], []
-    for _ in range(args.steps):
-        r = cpu_baseline()
-        vals.append(r["value"])
-        secs.append(r["seconds"])
-    v = statistics.median(vals)
-    T, K, N = CPU_SAMPLE["tokens"], CPU_SAMPLE["K"], CPU_SAMPLE["N"]
+        cpu_layer_step(T)
+    secs = [cpu_layer_step(T) for _ in range(args.steps)]
+    med = statistics.median(secs)
+    v = round(3 * 2.0 * T * HIDDEN * FFN / med / 1e12, 6)
+    cores = oracle.threads()
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOPS", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.median(secs) * 1e3, 1),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(med * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded numpy, same recipe as the fp8bs arm)",
-        "config": {"workload": WORKLOAD, "tokens": TOKENS, "K": HIDDEN, "N": FFN,
-                   "sample": f"tokens={T}, K={K}, N={N} per step"},
-        "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": 1, "kind": "oracle",
-                         "sample": f"layer step on tokens={T}, K={K}, N={N}"},
+        "data": DATA, "config": config_dict(world),
+        "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": _cpu_sample(T) + " per step"},
         "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -693,7 +729,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=0.0)
+    ap.add_argument("--ref-tokens", type=int, default=REFERENCE_STEP_TOKENS,
+                    help="tokens of the layer step the reference arm runs per step (multiple of 128)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "fp8bs":
         ap.error("at least 3 warm-up steps")

@@ -480,29 +480,47 @@ static int mx_group_exponent(float amax)
     return e;
 }
 
-/* x [R x K] row-major (ldx elements) -> q [R x K] (ldq bytes per row) and the
- * exponent bytes sf as described above.  K % 128 == 0. */
-void fp8bs_oracle_mx_quant_1x32(const void *x, int dtype, int64_t R, int64_t K, int64_t ldx,
-                                uint8_t *q, int64_t ldq, uint8_t *sf, int64_t ldsf)
+/* MX groups of rows r = t, t + nt, ... (one whole row per thread step). */
+struct mx_quant_job {
+    const void *x;
+    int dtype;
+    int64_t R, K, ldx;
+    uint8_t *q;
+    int64_t ldq;
+    uint8_t *sf;
+    int64_t ldsf;
+};
+
+static void mx_quant_rows(void *p, int t, int nt)
 {
-    for (int64_t r = 0; r < R; ++r) {
-        for (int64_t g = 0; g < K / 32; ++g) {
+    const struct mx_quant_job *j = (const struct mx_quant_job *)p;
+    for (int64_t r = t; r < j->R; r += nt) {
+        for (int64_t g = 0; g < j->K / 32; ++g) {
             float amax = 0.0f, mult;
             int e;
             for (int c = 0; c < 32; ++c) {
-                float a = fabsf(load_elem(x, dtype, ldx, r, g * 32 + c));
+                float a = fabsf(load_elem(j->x, j->dtype, j->ldx, r, g * 32 + c));
                 if (a > amax)
                     amax = a;
             }
             e = mx_group_exponent(amax);
             mult = ldexpf(1.0f, -e);       /* exact: 2^-127 .. 2^127 are binary32 values */
             for (int c = 0; c < 32; ++c) {
-                volatile float y = load_elem(x, dtype, ldx, r, g * 32 + c) * mult;
-                q[r * ldq + g * 32 + c] = fp8bs_oracle_e4m3_encode(y);
+                volatile float y = load_elem(j->x, j->dtype, j->ldx, r, g * 32 + c) * mult;
+                j->q[r * j->ldq + g * 32 + c] = fp8bs_oracle_e4m3_encode(y);
             }
-            sf[((g / 4) * ldsf + r) * 4 + g % 4] = (uint8_t)(e + 127);
+            j->sf[((g / 4) * j->ldsf + r) * 4 + g % 4] = (uint8_t)(e + 127);
         }
     }
+}
+
+/* x [R x K] row-major (ldx elements) -> q [R x K] (ldq bytes per row) and the
+ * exponent bytes sf as described above.  K % 128 == 0. */
+void fp8bs_oracle_mx_quant_1x32(const void *x, int dtype, int64_t R, int64_t K, int64_t ldx,
+                                uint8_t *q, int64_t ldq, uint8_t *sf, int64_t ldsf)
+{
+    struct mx_quant_job j = {x, dtype, R, K, ldx, q, ldq, sf, ldsf};
+    run_threads(mx_quant_rows, &j, R);
 }
 
 /* One output element of the MX GEMM

@@ -60,7 +60,7 @@ def test_reference_arm_line_under_torchrun(tmp_path):
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(port),
            os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
-           "--warmup", "0"]
+           "--warmup", "0", "--ref-tokens", "128"]
     out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
@@ -68,3 +68,6 @@ def test_reference_arm_line_under_torchrun(tmp_path):
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["config"] == bench.config_dict(2)          # the fp8bs arm's config, unchanged
+    assert d["cpu_baseline"]["cores"] == bench.host_cores()
+    assert "tokens=128" in d["cpu_baseline"]["sample"]

@@ -9,6 +9,7 @@ import torch
 
 import fp8_fine_grained_15_b300 as fb
 import oracle
+import full_ref
 from gpu_helpers import DEV, MODES, gemm_operands, to_dev_f32, to_dev_u8
 
 pytestmark = pytest.mark.gpu
@@ -69,3 +70,17 @@ def test_gemm_accumulate_zero_k_leaves_c():
     assert st == fb.FP8BS_OK
     assert fb.fp8bs_sync_status() == fb.FP8BS_OK
     assert torch.all(C == 3.5)
+
+
+def test_layer_wgrad_accumulate_full():
+    """The layer's Wgrad (7168 x 18432, K = 4096 tokens) added into an FP32
+    gradient buffer that already holds values, with the K split of the last
+    wave: every element of C_new - C_old against the oracle."""
+    A, sa, B, sb, mode, _ = full_ref.layer_gemm_args("wgrad")
+    M, N = A.shape[0], B.shape[0]
+    c0 = np.random.default_rng(17).standard_normal((M, N)).astype(np.float32) * np.float32(1e-2)
+    c1 = _acc(A, sa, B, sb, "PERCOL", c0, fb.fp8bs_gemm_workspace_size(M, N, A.shape[1]))
+    c_ref, s_abs = full_ref.layer_reference("wgrad")
+    err = np.abs(c1 - (c0.astype(np.float64) + c_ref))
+    bound = 1e-5 * s_abs + 2.0 ** -24 * np.abs(c1)
+    assert np.all(err <= bound), f"max err/bound {np.max(err / np.maximum(bound, 1e-300))}"

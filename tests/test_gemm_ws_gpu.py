@@ -3,7 +3,7 @@ along K over the idle CTA pairs, with the FP32 partials in a caller-provided
 workspace summed by a second kernel.  Parity with the CPU oracle under the
 same element-wise tolerance as fp8bs_gemm, on shapes that split (few tiles,
 long K), on smaller workspaces (fewer K-ranges, then none), and at the layer
-sizes; the split result is deterministic."""
+sizes on every output element; the split result is deterministic."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +12,7 @@ import fp8_fine_grained_15_b300 as fb
 import oracle
 from gpu_helpers import (DEV, MODES, assert_gemm_close, gemm_operands, gpu_gemm, gpu_gemm_ws,
                          to_dev_f32, to_dev_u8)
-from test_gemm_gpu import _tile_samples, layer  # noqa: F401  (module fixture)
+import full_ref
 
 pytestmark = pytest.mark.gpu
 
@@ -74,39 +74,12 @@ def test_gemm_ws_misaligned_workspace_rejected():
     assert st == fb.FP8BS_ERR_MISALIGNED
 
 
-def _tail_samples(M, N, n_samples, seed):
-    """Elements of the last tiles of the m-fastest walk (256 x 256 tiles): the
-    ones a split touches first."""
-    rng = np.random.default_rng(seed)
-    mt = (M + 255) // 256
-    nt = (N + 255) // 256
-    tiles = np.arange(mt * nt)[-min(24, mt * nt):]
-    t = rng.choice(tiles, n_samples)
-    rows = (t % mt) * 256 + rng.integers(0, 256, n_samples)
-    cols = (t // mt) * 256 + rng.integers(0, 256, n_samples)
-    keep = (rows < M) & (cols < N)
-    return rows[keep].astype(np.int64), cols[keep].astype(np.int64)
-
-
-def test_layer_dgrad_ws_sampled(layer):  # noqa: F811
-    d = layer
-    c = gpu_gemm_ws(d["dYq"], d["Sdy"], d["Wq"], d["Sw"], oracle.SB_BLOCK_NK, torch.bfloat16)
-    r1, c1 = _tile_samples(4096, 7168, seed=21, extra=2000)
-    r2, c2 = _tail_samples(4096, 7168, 3000, seed=22)
-    rows, cols = np.concatenate([r1, r2]), np.concatenate([c1, c2])
-    c_ref, s_abs = oracle.gemm_elements(d["dYq"], d["Sdy"], d["Wq"], d["Sw"],
-                                        oracle.SB_BLOCK_NK, rows, cols)
-    assert_gemm_close(c[rows, cols], c_ref, s_abs, True, "Dgrad ws 4096x7168x18432")
-    assert np.isfinite(c).all()
-
-
-def test_layer_wgrad_ws_sampled(layer):  # noqa: F811
-    d = layer
-    c = gpu_gemm_ws(d["XqT"], d["SxT"], d["dYqT"], d["SdyT"], oracle.SB_PERCOL, torch.float32)
-    r1, c1 = _tile_samples(7168, 18432, seed=23, extra=2000)
-    r2, c2 = _tail_samples(7168, 18432, 3000, seed=24)
-    rows, cols = np.concatenate([r1, r2]), np.concatenate([c1, c2])
-    c_ref, s_abs = oracle.gemm_elements(d["XqT"], d["SxT"], d["dYqT"], d["SdyT"],
-                                        oracle.SB_PERCOL, rows, cols)
-    assert_gemm_close(c[rows, cols], c_ref, s_abs, False, "Wgrad ws 7168x18432x4096")
-    assert np.isfinite(c).all()
+@pytest.mark.parametrize("which", ["fprop", "dgrad", "wgrad"])
+def test_layer_gemm_ws_full(which):
+    """The layer's GEMM through fp8bs_gemm_ws (the bench's call: the last,
+    partial wave split along K), every output element against the oracle."""
+    A, sa, B, sb, mode, bf16_out = full_ref.layer_gemm_args(which)
+    assert fb.fp8bs_gemm_workspace_size(A.shape[0], B.shape[0], A.shape[1]) > 0
+    c = gpu_gemm_ws(A, sa, B, sb, mode, torch.bfloat16 if bf16_out else torch.float32)
+    c_ref, s_abs = full_ref.layer_reference(which)
+    assert_gemm_close(c, c_ref, s_abs, bf16_out, f"layer {which} ws {c.shape}")

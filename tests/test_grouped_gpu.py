@@ -7,6 +7,7 @@ import torch
 import fp8_fine_grained_15_b300 as fb
 import oracle
 import workloads as wl
+import full_ref
 from gpu_helpers import DEV, assert_gemm_close, oracle_input, to_dev_f32, to_dev_u8
 
 pytestmark = pytest.mark.gpu
@@ -74,35 +75,15 @@ def test_grouped_bad_offsets_reported_and_nothing_written(offsets):
     assert fb.fp8bs_sync_status() == fb.FP8BS_OK      # the status was cleared
 
 
-def test_grouped_moe_up_projection_sampled():
+def test_grouped_moe_up_projection_full():
     """32 experts, 16384 routed rows with Zipf(1.1) counts padded to 128,
-    K = 7168, N = 4096 per expert."""
-    counts, offsets, x, w = wl.grouped_moe()
-    E, K, N = w.shape
-    Aq, sa = oracle.quant_act_1x128(oracle_input(x))
-    Bq = np.empty((E, N, K), np.uint8)
-    sb = np.empty((E, K // 128, N // 128), np.float32)
-    for e in range(E):
-        _, Bq[e], sb[e] = oracle.quant_w_128x128(oracle_input(w[e]), with_transpose=True)
+    K = 7168, N = 4096 per expert: every output element against the oracle
+    (padding rows must come out as exactly 0)."""
+    counts, offsets, Aq, sa, Bq, sb = full_ref.moe_operands()
     st, c = _run_grouped(offsets, Aq, sa, Bq, sb, fb.FP8BS_SB_BLOCK_KN)
     assert st == fb.FP8BS_OK
-    rng = np.random.default_rng(7)
-    rows, cols = [], []
-    for e in range(E):
-        r0, r1 = int(offsets[e]), int(offsets[e + 1])
-        real = r0 + int(counts[e])
-        for n0 in range(0, N, 256):               # one element per (m-tile, n-tile)
-            for m0 in range(r0, r1, 128):
-                rows.append(rng.integers(m0, m0 + 128))
-                cols.append(rng.integers(n0, n0 + 256))
-        if real < r1:                              # a padding row must come out as 0
-            rows.append(r1 - 1)
-            cols.append(rng.integers(0, N))
-    rows = np.array(rows, np.int64)
-    cols = np.array(cols, np.int64)
-    c_ref, s_abs = oracle.grouped_gemm_elements(offsets, Aq, sa, Bq, sb, oracle.SB_BLOCK_KN,
-                                                rows, cols)
-    assert_gemm_close(c[rows, cols], c_ref, s_abs, True, "grouped MoE")
-    pad_rows = [int(offsets[e]) + int(counts[e]) for e in range(E)
-                if int(offsets[e]) + int(counts[e]) < int(offsets[e + 1])]
-    assert np.all(c[pad_rows] == 0)
+    c_ref, s_abs = full_ref.moe_reference()
+    assert_gemm_close(c, c_ref, s_abs, True, "grouped MoE")
+    pad = np.concatenate([np.arange(int(offsets[e]) + int(counts[e]), int(offsets[e + 1]))
+                          for e in range(len(counts))])
+    assert pad.size > 0 and np.all(c[pad] == 0)

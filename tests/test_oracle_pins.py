@@ -337,7 +337,8 @@ def test_results_do_not_depend_on_the_thread_count():
             rows, cols = np.array([0, 5, 639, 17]), np.array([0, 255, 3, 100])
             ce, ae = oracle.gemm_elements(qT, sT, B, sb, oracle.SB_PERCOL, rows, cols)
             assert np.array_equal(ce, c[rows, cols]) and np.array_equal(ae, a[rows, cols])
-            outs.append((q, s, qT, sT, wq, wqT, ws, c, a))
+            mq, msf = oracle.mx_quant_1x32(xb)
+            outs.append((q, s, qT, sT, wq, wqT, ws, c, a, mq, msf))
     finally:
         oracle.set_threads(0)
     for other in outs[1:]:
