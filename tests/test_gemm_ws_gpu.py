@@ -77,9 +77,10 @@ def test_gemm_ws_misaligned_workspace_rejected():
 @pytest.mark.parametrize("which", ["fprop", "dgrad", "wgrad"])
 def test_layer_gemm_ws_full(which):
     """The layer's GEMM through fp8bs_gemm_ws (the bench's call: the last,
-    partial wave split along K), every output element against the oracle."""
+    partial wave split along K where the tile count leaves one -- Dgrad and
+    Wgrad on a 148-SM B300, not Fprop), every output element against the
+    oracle."""
     A, sa, B, sb, mode, bf16_out = full_ref.layer_gemm_args(which)
-    assert fb.fp8bs_gemm_workspace_size(A.shape[0], B.shape[0], A.shape[1]) > 0
     c = gpu_gemm_ws(A, sa, B, sb, mode, torch.bfloat16 if bf16_out else torch.float32)
     c_ref, s_abs = full_ref.layer_reference(which)
     assert_gemm_close(c, c_ref, s_abs, bf16_out, f"layer {which} ws {c.shape}")
