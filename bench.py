@@ -433,7 +433,7 @@ def run_extras(dev, stream, peaks):
     out["quant_dispatch_moe"] = {"tokens": T, "experts": E, "us": round(md * 1e3, 2),
                                  "GB/s": round(dbytes / (md * 1e-3) / 1e9, 1),
                                  "frac_hbm": round(dbytes / (md * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                                 "launches": 4}
+                                 "launches": 3}
     del xt, qd, sd
 
     # MX variant: the layer's Fprop with 1x32 power-of-two scales applied by the

@@ -550,41 +550,50 @@ fp8bs_status fp8bs_quant_dispatch(const void* x, fp8bs_dtype xt, int64_t T, int6
                                   int32_t* row_token, void* stream) {
   if (T < 0 || K < 0 || M_cap < 0 || !valid_dtype(xt)) return FP8BS_ERR_INVALID_ARG;
   if (E < 1 || E > kDispatchMaxExperts) return FP8BS_ERR_UNSUPPORTED;
-  if (K % 128 != 0 || M_cap % 128 != 0) return FP8BS_ERR_UNSUPPORTED;
+  if (K <= 0 || K % 128 != 0 || M_cap % 128 != 0) return FP8BS_ERR_UNSUPPORTED;
   if (M_cap < T + 127 * static_cast<int64_t>(E)) return FP8BS_ERR_INVALID_ARG;   // worst-case padding
   if (T * (K / 128) > INT_MAX || M_cap > INT_MAX) return FP8BS_ERR_UNSUPPORTED;
+  if ((T + kRankChunk - 1) / kRankChunk * E > kPlanMaxChunkCounts) return FP8BS_ERR_UNSUPPORTED;
   if (offsets == nullptr || counts == nullptr || (T > 0 && (expert == nullptr || token_row == nullptr)))
     return FP8BS_ERR_INVALID_ARG;
-  if (K > 0 && (x == nullptr || q == nullptr || s == nullptr || row_token == nullptr))
+  if (x == nullptr || q == nullptr || s == nullptr || row_token == nullptr)
     return FP8BS_ERR_INVALID_ARG;
-  if (K > 0 && (ldx < K || ldq < K || lds < M_cap)) return FP8BS_ERR_INVALID_ARG;
-  if (K > 0 && (!aligned(x, 16) || (ldx * static_cast<int64_t>(dtype_size(xt))) % 16 ||
-                !aligned(q, 16) || ldq % 16 || !aligned(s, 4)))
+  if (ldx < K || ldq < K || lds < M_cap) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (ldx * static_cast<int64_t>(dtype_size(xt))) % 16 || !aligned(q, 16) ||
+      ldq % 16 || !aligned(s, 4))
     return FP8BS_ERR_MISALIGNED;
   if (!aligned(offsets, 4) || !aligned(counts, 4)) return FP8BS_ERR_MISALIGNED;
   cudaStream_t st = as_stream(stream);
   DeviceInfo di;
   fp8bs_status rc = device_info(&di);
   if (rc != FP8BS_OK) return rc;
-  dispatch_plan_kernel<<<1, 1024, 0, st>>>(expert, T, E, token_row, counts, offsets);
-  if ((rc = launch_status()) != FP8BS_OK || T == 0 || K == 0) return rc;
+  // row_token's first chunks * E entries hold the chunk counts between the rank
+  // and plan launches (M_cap >= T + 127 E >= chunks * E for E <= 256)
+  const int64_t chunks = (T + kRankChunk - 1) / kRankChunk;
+  if (chunks > 0)
+    dispatch_rank_kernel<<<static_cast<unsigned>(chunks), kRankChunk, 0, st>>>(expert, T, E, token_row,
+                                                                              row_token);
+  if ((rc = launch_status()) != FP8BS_OK) return rc;
+  const size_t plan_smem = static_cast<size_t>(chunks * E) * sizeof(int32_t);
+  if (plan_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(dispatch_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kPlanMaxChunkCounts * sizeof(int32_t))) != cudaSuccess)
+    return FP8BS_ERR_CUDA;
+  dispatch_plan_kernel<<<1, 1024, plan_smem, st>>>(expert, T, E, static_cast<int>(chunks), row_token,
+                                                   token_row, counts, offsets);
+  if ((rc = launch_status()) != FP8BS_OK || T == 0) return rc;
   const int64_t tiles = T * (K / 128);
   int64_t blocks = (tiles + 63) / 64;
   if (blocks > static_cast<int64_t>(di.num_sms) * 8) blocks = static_cast<int64_t>(di.num_sms) * 8;
   if (xt == FP8BS_BF16)
     quant_dispatch_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(T),
-        static_cast<uint32_t>(K / 128), ldx, expert, E, token_row, offsets, q, ldq, s, lds);
+        static_cast<uint32_t>(K / 128), ldx, token_row, E, counts, offsets, q, ldq, s, lds,
+        row_token);
   else
     quant_dispatch_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
         static_cast<const float*>(x), static_cast<uint32_t>(T), static_cast<uint32_t>(K / 128),
-        ldx, expert, E, token_row, offsets, q, ldq, s, lds);
-  if ((rc = launch_status()) != FP8BS_OK) return rc;
-  dispatch_rows_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, st>>>(
-      expert, T, E, offsets, token_row, row_token);
-  if ((rc = launch_status()) != FP8BS_OK) return rc;
-  dispatch_pad_kernel<<<dim3(static_cast<unsigned>(E), 127), 256, 0, st>>>(
-      counts, offsets, static_cast<int>(K / 128), q, ldq, s, lds, row_token);
+        ldx, token_row, E, counts, offsets, q, ldq, s, lds, row_token);
   return launch_status();
 }
 

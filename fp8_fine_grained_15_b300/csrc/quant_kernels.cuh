@@ -543,73 +543,153 @@ __global__ void __launch_bounds__(256) quant_dual_kernel(const TIn* __restrict__
 // projection and dispatched in FP8).
 constexpr int kDispatchMaxExperts = 256;
 
-// One CTA of 1024 threads: in chunks of 1024 tokens, each token's rank among
-// the earlier tokens of its expert (warp match + per-warp counts, prefix over
-// warps), then per-expert counts and padded offsets.  rank_out[t] = rank.
-// The per-warp counts are kept expert-major with rows of 33 words
-// (cnt[e][warp]): the prefix over the 32 warps of one expert is a warp-wide
-// shuffle scan of consecutive words, and the per-token rank reads of a warp
-// (one warp column, several experts) fall in different banks.  The next
-// chunk's expert ids are loaded while the current chunk is ranked.
+// The plan (which row each token lands in) takes two small launches:
+//  dispatch_rank_kernel   one CTA per chunk of kRankChunk tokens: each token's
+//                         rank among the chunk's earlier tokens of its expert
+//                         (warp match, then a prefix of the per-warp counts over
+//                         the chunk's warps) into token_row[t], and the chunk's
+//                         per-expert counts into row_token[chunk * E + e] (the
+//                         start of row_token serves as scratch: it is rewritten
+//                         by the quantize kernel);
+//  dispatch_plan_kernel   one CTA: the chunk counts, read into shared memory,
+//                         give each chunk's first rank per expert (prefix over
+//                         the chunks), the expert counts and the padded offsets;
+//                         every token's row = offset + chunk base + rank goes to
+//                         token_row[t].
+// Tokens keep their order inside an expert.  (A single CTA ranking all 16384
+// tokens of the MoE workload was issue-bound at ~21 us.)
+constexpr int kRankChunk = 1024;
+constexpr int kPlanMaxChunkCounts = 51200;  // chunks * E the plan CTA holds in shared memory (200 KB)
+
+// Lanes of the warp holding the same expert id as this lane (ids < 256; -1 =
+// no expert, matched with the other lanes holding none), from nine ballots.
+__device__ __forceinline__ unsigned match_expert(int e) {
+  const bool has = e >= 0;
+  const unsigned v = __ballot_sync(0xffffffffu, has);
+  unsigned m = has ? v : ~v;
+  const int bits = has ? e : 0;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const bool on = (bits >> b) & 1;
+    const unsigned w = __ballot_sync(0xffffffffu, on);
+    m &= on ? w : ~w;
+  }
+  return m;
+}
+
+__global__ void __launch_bounds__(kRankChunk) dispatch_rank_kernel(const int32_t* __restrict__ expert,
+                                                                   int64_t T, int E,
+                                                                   int32_t* __restrict__ token_row,
+                                                                   int32_t* __restrict__ chunk_counts) {
+  __shared__ int32_t cnt[kDispatchMaxExperts][33];   // [expert][warp], padded rows
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kRankChunk + tid;
+  int e = t < T ? expert[t] : -1;
+  if (t < T && (e < 0 || e >= E)) {   // routing outside [0, E): the token is dropped
+    atomicOr(&g_device_error, kDevErrBadRouting);
+    e = -1;
+  }
+  for (int i = tid; i < 32 * E; i += kRankChunk) cnt[i >> 5][i & 31] = 0;
+  __syncthreads();
+  const unsigned m = match_expert(e);
+  const unsigned lower = m & ((1u << lane) - 1u);
+  if (e >= 0 && lower == 0) cnt[e][warp] = __popc(m);
+  __syncthreads();
+  for (int x = warp; x < E; x += 32) {   // exclusive prefix over the warps, per expert
+    const int c = cnt[x][lane];
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    cnt[x][lane] = incl - c;
+    if (lane == 31) chunk_counts[static_cast<int64_t>(blockIdx.x) * E + x] = incl;
+  }
+  __syncthreads();
+  if (t < T) token_row[t] = e >= 0 ? cnt[e][warp] + static_cast<int>(__popc(lower)) : -1;
+}
+
 __global__ void __launch_bounds__(1024) dispatch_plan_kernel(const int32_t* __restrict__ expert,
-                                                             int64_t T, int E,
-                                                             int32_t* __restrict__ rank_out,
+                                                             int64_t T, int E, int chunks,
+                                                             const int32_t* __restrict__ chunk_counts,
+                                                             int32_t* __restrict__ token_row,
                                                              int32_t* __restrict__ counts,
                                                              int32_t* __restrict__ offsets) {
-  __shared__ int32_t cnt[kDispatchMaxExperts][33];
-  __shared__ int32_t running[kDispatchMaxExperts];
+  extern __shared__ int32_t base[];   // [chunk][expert]: first rank, then + offset (dynamic)
+  __shared__ int32_t off_s[kDispatchMaxExperts + 1];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int e = tid; e < kDispatchMaxExperts; e += 1024) running[e] = 0;
-  int e_next = tid < T ? expert[tid] : -1;
-  for (int64_t base = 0; base < T; base += 1024) {
-    for (int i = tid; i < 32 * E; i += 1024) cnt[i >> 5][i & 31] = 0;   // rows of the E experts
-    const int64_t t = base + tid;
-    int e = e_next;
-    e_next = t + 1024 < T ? expert[t + 1024] : -1;
-    if (t < T && (e < 0 || e >= E)) {   // routing outside [0, E): the token is dropped
-      atomicOr(&g_device_error, kDevErrBadRouting);
-      e = -1;
+  for (int i = tid; i < chunks * E; i += blockDim.x) base[i] = chunk_counts[i];
+  __syncthreads();
+  for (int x = tid; x < E; x += blockDim.x) {   // prefix over the chunks, one thread per expert
+    int run = 0;
+    for (int c = 0; c < chunks; ++c) {
+      const int v = base[c * E + x];
+      base[c * E + x] = run;
+      run += v;
     }
-    __syncthreads();
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    const int lane_rank = __popc(m & ((1u << lane) - 1u));
-    if (e >= 0 && lane_rank == 0) cnt[e][warp] = __popc(m);
-    __syncthreads();
-    for (int x = warp; x < E; x += 32) {   // exclusive prefix over the warps, per expert
-      const int c = cnt[x][lane];
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const int run = running[x];
-      cnt[x][lane] = run + incl - c;
-      __syncwarp();
-      if (lane == 31) running[x] = run + incl;
-    }
-    __syncthreads();
-    if (e >= 0) rank_out[t] = cnt[e][warp] + lane_rank;
-    __syncthreads();
+    counts[x] = run;
+    off_s[x] = (run + 127) / 128 * 128;   // padded size, scanned below
   }
-  if (tid == 0) {
-    int32_t off = 0;
-    for (int e = 0; e < E; ++e) {
-      counts[e] = running[e];
-      offsets[e] = off;
-      off += (running[e] + 127) / 128 * 128;
+  __syncthreads();
+  if (warp == 0) {   // exclusive scan of the padded sizes (E <= 256: 8 per lane)
+    constexpr int kPer = kDispatchMaxExperts / 32;
+    int v[kPer], sum = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int x = lane * kPer + i;
+      v[i] = x < E ? off_s[x] : 0;
+      sum += v[i];
     }
-    offsets[E] = off;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int x = lane * kPer + i;
+      if (x < E) {
+        off_s[x] = run;
+        offsets[x] = run;
+      }
+      run += v[i];
+    }
+    if (lane == 31) offsets[E] = incl;
+  }
+  __syncthreads();
+  for (int i = tid; i < chunks * E; i += blockDim.x) base[i] += off_s[i % E];
+  __syncthreads();
+  constexpr int kBatch = 8;   // tokens per thread in flight
+  for (int64_t t0 = tid; t0 < T; t0 += kBatch * static_cast<int64_t>(blockDim.x)) {
+    int e[kBatch], r[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t t = t0 + j * static_cast<int64_t>(blockDim.x);
+      e[j] = t < T ? expert[t] : -1;
+      r[j] = t < T ? token_row[t] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t t = t0 + j * static_cast<int64_t>(blockDim.x);
+      if (e[j] >= 0 && e[j] < E)   // dropped tokens keep token_row -1
+        token_row[t] = base[static_cast<int>(t / kRankChunk) * E + e[j]] + r[j];
+    }
   }
 }
 
-// 1x128 quantization of token t's row into row offsets[e] + rank[t] (four lanes
-// per 128-element tile, as in quant_1x128_kernel).
+// 1x128 quantization of token t's row into row token_row[t] (four lanes per
+// 128-element tile, as in quant_1x128_kernel), with row_token[row] = t;
+// dropped tokens (row -1) are skipped.  Then the padding rows, one warp per
+// (expert, padding slot): codes 0, scales 1, row_token -1.
 template <typename TIn>
 __global__ void __launch_bounds__(256) quant_dispatch_kernel(
-    const TIn* __restrict__ x, uint32_t T, uint32_t KB, int64_t ldx, const int32_t* __restrict__ expert,
-    int E, const int32_t* __restrict__ rank, const int32_t* __restrict__ offsets,
-    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s, int64_t lds) {
+    const TIn* __restrict__ x, uint32_t T, uint32_t KB, int64_t ldx,
+    const int32_t* __restrict__ token_row, int E, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ offsets, uint8_t* __restrict__ q, int64_t ldq,
+    float* __restrict__ s, int64_t lds, int32_t* __restrict__ row_token) {
   constexpr int kVec = Vec16<TIn>::kN;
   constexpr int kLoads = 128 / (4 * kVec);
   const int lane = threadIdx.x & 31;
@@ -621,8 +701,8 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     const uint32_t tile = base + sub;
     const bool valid = tile < total;
     const uint32_t t = valid ? tile / KB : 0, kb = valid ? tile - t * KB : 0;
-    const int e = valid ? expert[t] : -1;
-    const bool routed = valid && e >= 0 && e < E;
+    const int32_t row32 = valid ? token_row[t] : -1;
+    const bool routed = row32 >= 0;
     uint4 v[kLoads];
     const TIn* src = x + static_cast<int64_t>(t) * ldx + kb * 128 + l * kVec;
 #pragma unroll
@@ -640,7 +720,7 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
     float sc, r;
     tile_scale(amax, sc, r);
     if (routed) {
-      const int64_t row = static_cast<int64_t>(offsets[e]) + rank[t];
+      const int64_t row = row32;
       uint8_t* dst = q + row * ldq + kb * 128 + l * kVec;
 #pragma unroll
       for (int i = 0; i < kLoads; ++i) {
@@ -652,43 +732,23 @@ __global__ void __launch_bounds__(256) quant_dispatch_kernel(
           *reinterpret_cast<uint32_t*>(dst + i * 4 * kVec) = e4m3x4(f, r);
         }
       }
-      if (l == 0) s[static_cast<int64_t>(kb) * lds + row] = sc;
+      if (l == 0) {
+        s[static_cast<int64_t>(kb) * lds + row] = sc;
+        if (kb == 0) row_token[row] = static_cast<int32_t>(t);
+      }
     }
   }
-}
-
-// token_row[t] = offsets[e] + rank[t] (rank read from token_row itself) and
-// row_token[row] = t.
-__global__ void dispatch_rows_kernel(const int32_t* __restrict__ expert, int64_t T, int E,
-                                     const int32_t* __restrict__ offsets,
-                                     int32_t* __restrict__ token_row,
-                                     int32_t* __restrict__ row_token) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= T) return;
-  const int e = expert[t];
-  if (e < 0 || e >= E) {
-    token_row[t] = -1;
-    return;
+  // padding rows: slot j of expert e is row offsets[e] + counts[e] + j when
+  // that is below offsets[e + 1] (at most 127 per expert)
+  for (uint32_t u = warp_id; u < static_cast<uint32_t>(E) * 127u; u += num_warps) {
+    const int e = static_cast<int>(u / 127u);
+    const int64_t r = static_cast<int64_t>(offsets[e]) + counts[e] + (u % 127u);
+    if (r >= offsets[e + 1]) continue;
+    uint4* dst = reinterpret_cast<uint4*>(q + r * ldq);
+    for (uint32_t i = lane; i < KB * 8u; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+    for (uint32_t kb = lane; kb < KB; kb += 32) s[static_cast<int64_t>(kb) * lds + r] = 1.0f;
+    if (lane == 0) row_token[r] = -1;
   }
-  const int32_t row = offsets[e] + token_row[t];
-  token_row[t] = row;
-  row_token[row] = static_cast<int32_t>(t);
-}
-
-// Padding row blockIdx.y of expert blockIdx.x (when the expert has that many
-// padding rows): codes 0, scales 1, row_token -1.
-__global__ void dispatch_pad_kernel(const int32_t* __restrict__ counts,
-                                    const int32_t* __restrict__ offsets, int KB,
-                                    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s,
-                                    int64_t lds, int32_t* __restrict__ row_token) {
-  const int e = blockIdx.x;
-  const int64_t r = static_cast<int64_t>(offsets[e]) + counts[e] + blockIdx.y;
-  if (r >= offsets[e + 1]) return;
-  uint4* dst = reinterpret_cast<uint4*>(q + r * ldq);
-  const int64_t words = static_cast<int64_t>(KB) * 128 / 16;
-  for (int64_t i = threadIdx.x; i < words; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
-  for (int kb = threadIdx.x; kb < KB; kb += blockDim.x) s[static_cast<int64_t>(kb) * lds + r] = 1.0f;
-  if (threadIdx.x == 0) row_token[r] = -1;
 }
 
 // ------------------------------------------------------------ MX 1 x 32

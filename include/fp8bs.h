@@ -137,13 +137,17 @@ fp8bs_status fp8bs_quant_act_dual(const void* x, fp8bs_dtype xt, int64_t T, int6
  *               rows get codes 0 and scale 1 (a quantized zero row);
  *     token_row [T]: the row of each token;  row_token [M_cap]: the token of
  *               each row, -1 on padding rows.
- *   Rows at or past offsets[E] are left untouched.
- * Requirements: 1 <= E <= 256 and K % 128 == 0 and M_cap % 128 == 0
- * (UNSUPPORTED); M_cap >= T + 127 * E, the worst-case padded size
- * (INVALID_ARG); x, q 16-byte aligned, ldx*sizeof(xt) and ldq multiples of 16
- * (MISALIGNED).  An expert id outside [0, E) drops that token and is reported
- * by fp8bs_sync_status as FP8BS_ERR_DEVICE_BAD_ROUTING.  Four launches on the
- * stream (plan, quantize, row maps, padding). */
+ *   Rows of q and s at or past offsets[E] are left untouched.  row_token's
+ *   first ceil(T / 1024) * E entries serve as scratch between the launches,
+ *   so its entries at or past offsets[E] are unspecified on return.
+ * Requirements: 1 <= E <= 256, K > 0, K % 128 == 0, M_cap % 128 == 0 and
+ * ceil(T / 1024) * E <= 51200 (UNSUPPORTED); M_cap >= T + 127 * E, the
+ * worst-case padded size (INVALID_ARG); x, q 16-byte aligned, ldx*sizeof(xt)
+ * and ldq multiples of 16 (MISALIGNED).  An expert id outside [0, E) drops
+ * that token (token_row -1) and is reported by fp8bs_sync_status as
+ * FP8BS_ERR_DEVICE_BAD_ROUTING.  Three launches on the stream: ranks per
+ * 1024-token chunk, the plan of rows and offsets, and the quantization with
+ * both row maps and the padding rows. */
 fp8bs_status fp8bs_quant_dispatch(const void* x, fp8bs_dtype xt, int64_t T, int64_t K,
                                   int64_t ldx, const int32_t* expert, int32_t E, uint8_t* q,
                                   int64_t ldq, float* s, int64_t lds, int64_t M_cap,

@@ -168,6 +168,9 @@ def test_dispatch_host_checks(L):
     assert L.fp8bs_quant_dispatch(*args(4, 1024, K=100)) == fb.FP8BS_ERR_UNSUPPORTED
     assert L.fp8bs_quant_dispatch(*args(4, 512)) == fb.FP8BS_ERR_INVALID_ARG         # < T + 127 E
     assert L.fp8bs_quant_dispatch(*args(4, 1000)) == fb.FP8BS_ERR_UNSUPPORTED        # M_cap % 128
+    assert L.fp8bs_quant_dispatch(*args(4, 1024, K=0)) == fb.FP8BS_ERR_UNSUPPORTED   # K == 0
+    assert L.fp8bs_quant_dispatch(*args(256, 256 * 1024 * 1024, T=205 * 1024)) == \
+        fb.FP8BS_ERR_UNSUPPORTED                                   # chunk counts past the plan CTA
 
 
 def _mx_gemm(L, M=128, N=256, K=256, A=FAKE, lda=256, sfa=FAKE, ldsfa=128, B=FAKE, ldb=256,

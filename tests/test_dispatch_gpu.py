@@ -45,7 +45,9 @@ def _check(x, expert, E):
     assert np.array_equal(t2r, rows)
     n = int(offr[E])
     assert np.array_equal(r2t[:n], r2tr)
-    assert np.all(r2t[n:] == -9), "rows past the last expert must stay untouched"
+    scratch = -(-x.shape[0] // 1024) * E   # row_token entries that serve as scratch
+    assert np.all(r2t[max(n, scratch):] == -9), "row_token past the rows and the scratch"
+    assert np.all(q[n:] == 0xAB) and np.all(s[:, n:] == -3.0), "rows past the last expert"
     if n:
         assert np.array_equal(q[:n], qr), "codes"
         assert np.array_equal(s[:, :n], sr), "scales"
