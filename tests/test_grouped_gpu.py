@@ -61,6 +61,26 @@ def test_grouped_nk_scales_fp32_out():
     assert_gemm_close(c, c_ref, s_abs, False, "grouped NK fp32")
 
 
+def test_grouped_odd_blocks_and_many_experts():
+    """Experts with odd numbers of 128-row blocks (the second half of their
+    last 256-row pair tile lies past the expert and must stay untouched), and
+    more experts than the pair kernel stages (300: the single-CTA kernel)."""
+    N, K = 256, 256
+    for E, sizes in ((5, [384, 128, 0, 640, 256]), (300, [128 if e % 97 == 0 else 0
+                                                            for e in range(300)])):
+        offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+        M_cap = int(offsets[-1]) + 256
+        a = wl.random_matrix((M_cap, K), seed=E + 50, dtype=torch.bfloat16)
+        Aq, sa = oracle.quant_act_1x128(oracle_input(a))
+        Bq, sb = _experts(E, N, K, seed=E + 51)
+        st, c = _run_grouped(offsets, Aq, sa, Bq, sb, fb.FP8BS_SB_BLOCK_KN)
+        assert st == fb.FP8BS_OK
+        n = int(offsets[-1])
+        c_ref, s_abs = oracle.grouped_gemm(offsets, Aq, sa, Bq, sb, oracle.SB_BLOCK_KN)
+        assert_gemm_close(c[:n], c_ref[:n], s_abs[:n], True, f"grouped E={E}")
+        assert np.all(c[n:] == 3.0), "rows past offsets[E] must be untouched"
+
+
 @pytest.mark.parametrize("offsets", [[0, 100, 256], [0, 256, 128], [128, 256, 384],
                                      [0, 128, 1024]])
 def test_grouped_bad_offsets_reported_and_nothing_written(offsets):
