@@ -99,6 +99,33 @@ int pair_clusters(K kernel) {
   return d.pair_clusters;
 }
 
+// How many 2-CTA clusters of the MX pair GEMM fit on the device at once
+// (queried once per device).
+template <typename K>
+int mx_pair_clusters(K kernel) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  static int cached[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (cached[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 512, 1, 1);
+    cfg.blockDim = dim3(kMxThreads, 1, 1);
+    cfg.dynamicSmemBytes = kMxPairSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 fp8bs_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
   std::lock_guard<std::mutex> lock(g_mutex);
   if (g_encode == nullptr) {
@@ -826,8 +853,9 @@ fp8bs_status fp8bs_mx_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, in
   if (st != FP8BS_OK) return st;
   CUtensorMap ta, tb, tsa, tsb, tc;
   const int64_t KB = K / kBK;
+  // CTA pairs: each CTA loads its 128 rows of A and half of the B tile
   if ((st = make_map_2d(&ta, A, K, M, lda, kBM)) != FP8BS_OK) return st;
-  if ((st = make_map_2d(&tb, B, K, N, ldb, kBN)) != FP8BS_OK) return st;
+  if ((st = make_map_2d(&tb, B, K, N, ldb, kBN / 2)) != FP8BS_OK) return st;
   if ((st = make_map_sf(&tsa, sfa, M, KB, ldsfa, kBM)) != FP8BS_OK) return st;
   if ((st = make_map_sf(&tsb, sfb, N, KB, ldsfb, kBN)) != FP8BS_OK) return st;
   if ((st = make_map_out(&tc, C, ct, N, M, ldc)) != FP8BS_OK) return st;
@@ -835,18 +863,23 @@ fp8bs_status fp8bs_mx_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* A, in
   p.M = static_cast<int32_t>(M);
   p.N = static_cast<int32_t>(N);
   p.KB = static_cast<int32_t>(KB);
-  p.num_m_tiles = static_cast<int32_t>((M + kBM - 1) / kBM);
+  p.num_m_tiles = static_cast<int32_t>((M + kPairTileM - 1) / kPairTileM);
   p.num_n_tiles = static_cast<int32_t>((N + kBN - 1) / kBN);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
-  const int grid = tiles < di.num_sms ? tiles : di.num_sms;
   auto run = [&](auto kernel) -> fp8bs_status {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kMxSmemBytes)) != cudaSuccess)
+                             static_cast<int>(kMxPairSmemBytes)) != cudaSuccess)
       return FP8BS_ERR_CUDA;
-    kernel<<<grid, kMxThreads, kMxSmemBytes, as_stream(stream)>>>(p, ta, tb, tsa, tsb, tc);
+    const int clusters = mx_pair_clusters(kernel);
+    if (clusters <= 0) return FP8BS_ERR_CUDA;
+    const int grid_clusters = tiles < clusters ? tiles : clusters;
+    kernel<<<2 * grid_clusters, kMxThreads, kMxPairSmemBytes, as_stream(stream)>>>(p, ta, tb, tsa,
+                                                                                   tsb, tc);
     return launch_status();
   };
-  return ct == FP8BS_BF16 ? run(fp8bs_mx_gemm_kernel<true>) : run(fp8bs_mx_gemm_kernel<false>);
+  return ct == FP8BS_BF16 ? run(fp8bs_mx_gemm_pair_kernel<true>)
+                          : run(fp8bs_mx_gemm_pair_kernel<false>);
+
 }
 
 fp8bs_status fp8bs_debug_timeout_probe(int64_t limit_ns, void* stream) {

@@ -409,16 +409,20 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n) {
 // ------------------------------------------------ block-scaled MMA (MX variant)
 
 // D[tmem] (+)= (A * B^T) with per-32-deep-group power-of-two scales applied
-// by the tensor core: A, B E4M3 in shared memory, one UE8M0 scale per row of
-// A and per row of B for this K=32 step, read from TMEM at sfa_tmem / sfb_tmem
-// (byte `sf id` of each 32-bit cell, the id carried in idesc).  One thread.
-__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                             uint32_t accumulate) {
+// by the tensor core, on CTA pairs (cta_group::2, issued by one thread of the
+// even CTA): A, B E4M3 in shared memory (rows split between the two CTAs), one
+// UE8M0 scale per row of A and per row of B for this K=32 step, read from
+// TMEM at sfa_tmem / sfb_tmem (byte `sf id` of each 32-bit cell, the id
+// carried in idesc); D in both CTAs' TMEM, and each CTA's scale cells read
+// from its own TMEM at the same columns.
+__device__ __forceinline__ void mma_mxf8f6f4_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                  uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
       "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");

@@ -103,13 +103,15 @@ def test_mx_quant_layer_activations_full_size():
 
 # ----------------------------------------------------------------------- GEMM
 
-def test_mx_gemm_single_group_applies_that_groups_exponents():
+@pytest.mark.parametrize("M,N", [(128, 256), (256, 256), (384, 512)])
+def test_mx_gemm_single_group_applies_that_groups_exponents(M, N):
     """Only group g holds non-zero codes (all 1.0); every row of A and of B has
     its own exponent in every group, so each output is exactly
     32 * 2^(ea(m, g) + eb(n, g)) -- it names the two scale bytes the tensor
-    core applied (row, column and group)."""
-    rng = np.random.default_rng(31)
-    M, N, K = 128, 256, 512
+    core applied (row, column and group), on both CTAs of a pair tile and in
+    both halves of B."""
+    rng = np.random.default_rng(31 + M + N)
+    K = 512
     sfa = rng.integers(100, 150, (K // 128, M, 4)).astype(np.uint8)
     sfb = rng.integers(100, 150, (K // 128, N, 4)).astype(np.uint8)
     for g in (0, 1, 2, 3, 6, 13):
