@@ -66,19 +66,20 @@ def dual_bytes(elems: int, in_bytes: int) -> float:
 
 
 # DRAM traffic per launch measured by ncu (dram__bytes_read.sum + write.sum), with
-# the sha256 of the kernel source it was measured on; ignored once the source changes.
+# the sha256 of the kernel sources it was measured on; ignored once they change.
 NCU_TRAFFIC = {
-    # ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch of
-    # `bench.py --case wgrad`, measured by ncu on that one launch
-    "gemm_wgrad": {"file": "gemm_pair_kernel.cuh", "src": "04c1dbfdadbd7d84",
-                   "bytes": 191641344 + 496067328},
+    # one launch of `bench.py --case wgrad`, measured by ncu on that launch
+    "gemm_wgrad": {"files": ("gemm_pair_kernel.cuh", "gemm_kernel.cuh", "ptx.cuh"),
+                   "src": "e6eb0db0803c0096", "bytes": 196612608 + 496589824},
 }
 
 
-def _src_hash(name: str) -> str:
-    p = os.path.join(ROOT, "fp8_fine_grained_15_b300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def _src_hash(names) -> str:
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "fp8_fine_grained_15_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def _peaks():
@@ -279,7 +280,7 @@ def run_fp8bs(args, rank, world, dist_on):
         peak, unit = peaks["hbm_gbs"], "GB/s"
     traffic = None
     rec = NCU_TRAFFIC.get(dom_name)
-    if rec and rec["src"] == _src_hash(rec["file"]):
+    if rec and rec["bytes"] is not None and rec["src"] == _src_hash(rec["files"]):
         traffic = rec["bytes"]
     roofline = {"bound": kind, "kernel": dom_name, "achieved": round(ach, 2),
                 "peak": round(peak, 1), "unit": unit, "frac": round(ach / peak, 4),
