@@ -52,6 +52,7 @@ struct DeviceInfo {
   bool init = false;
   int num_sms = 0;
   int pair_clusters = 0;   // co-resident 2-CTA clusters of the pair GEMM
+  int l2_bytes = 0;
 };
 
 std::mutex g_mutex;
@@ -64,7 +65,8 @@ fp8bs_status device_info(DeviceInfo* out) {
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceInfo& d = g_dev[dev];
   if (!d.init) {
-    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
       return FP8BS_ERR_CUDA;
     d.init = true;
   }
@@ -461,6 +463,15 @@ fp8bs_status gemm_dense(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
                                                                            : kPairGroupM;
   int clusters = 0;
   if ((st = pair_cluster_count(&clusters)) != FP8BS_OK) return st;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != FP8BS_OK) return st;
+  {
+    // operand panels a wave of clusters reads: its group's A panels and the
+    // B panels of its n tiles, each 256 rows x K bytes
+    const int64_t n_per_wave = (clusters + p.group_m - 1) / p.group_m;
+    const int64_t wave_bytes = (p.group_m + n_per_wave) * static_cast<int64_t>(kPairTileM) * K;
+    p.k_serpentine = wave_bytes > di.l2_bytes / 2 ? 1 : 0;
+  }
   const SplitPlan sp = plan_split(p.num_m_tiles * p.num_n_tiles, p.KB, clusters,
                                   ws != nullptr ? ws_bytes : 0, bn);
   p.full_tiles = sp.full_tiles;

@@ -82,6 +82,7 @@ struct GemmParams {
   int32_t splits;
   int32_t units;
   int32_t group_m;   // pair kernel: m tiles per group of the tile walk (>= 1)
+  int32_t k_serpentine;  // pair kernel: whole tiles of odd waves walk K downwards
 };
 
 struct GemmSmem {
