@@ -470,7 +470,7 @@ fp8bs_status gemm_dense(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
     // B panels of its n tiles, each 256 rows x K bytes
     const int64_t n_per_wave = (clusters + p.group_m - 1) / p.group_m;
     const int64_t wave_bytes = (p.group_m + n_per_wave) * static_cast<int64_t>(kPairTileM) * K;
-    p.k_serpentine = wave_bytes > di.l2_bytes / 2 ? 1 : 0;
+    p.k_order = wave_bytes > di.l2_bytes / 2 ? kKOrderSerpentine : kKOrderForward;
   }
   const SplitPlan sp = plan_split(p.num_m_tiles * p.num_n_tiles, p.KB, clusters,
                                   ws != nullptr ? ws_bytes : 0, bn);

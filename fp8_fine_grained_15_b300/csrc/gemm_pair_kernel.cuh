@@ -99,6 +99,7 @@ __device__ __forceinline__ void pair_tile_mn(int t, const GemmParams& p, int& mt
 struct PairUnit {
   int tile, kb0, kb1;
   int slot;   // < 0: whole tile, stored to C; else the partial's workspace slot
+  int rev;    // slabs taken last to first
 };
 
 __device__ __forceinline__ PairUnit pair_unit(int u, const GemmParams& p) {
@@ -108,6 +109,7 @@ __device__ __forceinline__ PairUnit pair_unit(int u, const GemmParams& p) {
     w.kb0 = 0;
     w.kb1 = p.KB;
     w.slot = -1;
+    w.rev = p.k_order == kKOrderSerpentine && ((u / static_cast<int>(gridDim.x >> 1)) & 1);
   } else {
     const int v = u - p.full_tiles;
     const int sp = v % p.splits;
@@ -115,19 +117,17 @@ __device__ __forceinline__ PairUnit pair_unit(int u, const GemmParams& p) {
     w.kb0 = (sp * p.KB) / p.splits;
     w.kb1 = ((sp + 1) * p.KB) / p.splits;
     w.slot = v;
+    w.rev = 0;
   }
   return w;
 }
 
-// Slab order of unit u: with p.k_serpentine, the whole tiles of every odd
-// wave of the persistent walk take their K slabs last to first.  A wave's
-// tiles share A panels with the previous wave's (same m group) and so start
-// on the slabs that wave read last, which are still in L2 when the panels of
-// a wave are too large to stay there whole (the K = 18432 Dgrad: 0.453 ->
-// 0.420 ms, measured).  The promotion's FP32 sum then runs over the slabs in
-// the reverse order.
-__device__ __forceinline__ bool pair_k_reversed(int u, const PairUnit& w, const GemmParams& p) {
-  return p.k_serpentine && w.slot < 0 && ((u / static_cast<int>(gridDim.x >> 1)) & 1);
+// K slab of the unit's i-th step (kb0 <= i <= kb1; i = kb1 gives the slab
+// after the last one, whose scales are prefetched and not used: kb1, or kb0 - 1
+// when reversed, either of which the scale loads treat as out of range when it
+// lies outside [0, KB)).
+__device__ __forceinline__ int pair_kb(const PairUnit& w, int i) {
+  return w.rev ? w.kb1 - 1 - (i - w.kb0) : i;
 }
 
 // Sum of the K-range partials of the tail tiles, in split order, converted to
@@ -234,9 +234,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         pair_tile_mn(w.tile, p, mt, nt);
         const int a_row = mt * kPairTileM + static_cast<int>(rank) * kBM;
         const int b_row = nt * BN + static_cast<int>(rank) * (BN / 2);
-        const bool rev = pair_k_reversed(u, w, p);
         for (int i = w.kb0; i < w.kb1; ++i) {
-          const int kb = rev ? w.kb1 - 1 - (i - w.kb0) : i;
+          const int kb = pair_kb(w, i);
           if (!bounded_wait(&sm.done[stage], phase ^ 1u, abort_flag)) {
             aborted = true;
             break;
@@ -320,41 +319,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
       for (int i = 0; i < Cfg::kWarpCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
+      // slab kb's scales; 0 for a slab outside [0, KB) (the one after a unit's last)
+      auto in_k = [&](int kb) { return static_cast<unsigned>(kb) < static_cast<unsigned>(p.KB); };
       auto load_sa = [&](int kb) -> float {
-        return (row_ok && static_cast<unsigned>(kb) < static_cast<unsigned>(p.KB)) ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ldsa + row)
-                                     : 0.0f;
+        return (row_ok && in_k(kb)) ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ldsa + row) : 0.0f;
       };
       // block mode: this warp's column block of B scales (one pointer kept)
       const float* sb_blk = p.sb + static_cast<int64_t>(col0 / 128) * p.sb_n_stride;
       auto load_sb = [&](int kb) -> float {
         if constexpr (kSb == kSbBlock) {
-          return (cols_ok && static_cast<unsigned>(kb) < static_cast<unsigned>(p.KB)) ? __ldg(sb_blk + static_cast<int64_t>(kb) * p.sb_k_stride)
-                                        : 0.0f;
+          return (cols_ok && in_k(kb)) ? __ldg(sb_blk + static_cast<int64_t>(kb) * p.sb_k_stride)
+                                       : 0.0f;
         } else {
           return 0.0f;
         }
       };
-      const bool rev = pair_k_reversed(u, w, p);
-      const int kstep = rev ? -1 : 1;
-      const int kfirst = rev ? w.kb1 - 1 : w.kb0;
+      const int kfirst = pair_kb(w, w.kb0);
       float sa_cur = load_sa(kfirst), sb_cur = load_sb(kfirst);
       // per-column mode: this warp's 128 B scales of a slab, staged in smem
       float* sb_mine = &sm.sb_stage[warp - 4][0][0];
       auto fetch_sb_cols = [&](int kb) -> float4 {
         const int c = col0 + lane * 4;
-        return (static_cast<unsigned>(kb) < static_cast<unsigned>(p.KB) && c < p.N)
+        return (in_k(kb) && c < p.N)
                    ? __ldg(reinterpret_cast<const float4*>(p.sb + static_cast<int64_t>(kb) * p.ldsb + c))
                    : make_float4(0.f, 0.f, 0.f, 0.f);
       };
       if constexpr (kSb == kSbPerCol) {
         const float4 v = fetch_sb_cols(kfirst);
-        reinterpret_cast<float4*>(sb_mine + (kfirst & 1) * 128)[lane] = v;
+        reinterpret_cast<float4*>(sb_mine + (w.kb0 & 1) * 128)[lane] = v;
         __syncwarp();
       }
-      for (int i = w.kb0, kb = kfirst; i < w.kb1; ++i, kb += kstep) {
-        const float sa_nxt = load_sa(kb + kstep), sb_nxt = load_sb(kb + kstep);
+      for (int i = w.kb0; i < w.kb1; ++i) {
+        const int kb_nxt = pair_kb(w, i + 1);
+        const float sa_nxt = load_sa(kb_nxt), sb_nxt = load_sb(kb_nxt);
         float4 sbc_nxt;
-        if constexpr (kSb == kSbPerCol) sbc_nxt = fetch_sb_cols(kb + kstep);
+        if constexpr (kSb == kSbPerCol) sbc_nxt = fetch_sb_cols(kb_nxt);
         if (!bounded_wait(&sm.done[stage], phase, abort_flag)) goto epilogue_done;
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) +
@@ -377,7 +376,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         } else {
           // columns past N carry zero scales (and zero products), so no guard is needed
           const float2 sa2 = make_float2(sa_cur, sa_cur);
-          const float* sbs = sb_mine + (kb & 1) * 128;
+          const float* sbs = sb_mine + (i & 1) * 128;   // staged by step, not by slab
 #pragma unroll
           for (int c = 0; c < Cfg::kChunks; c += 2) {
             tmem_ld32(taddr + (c + 1) * 32, rb);
@@ -387,7 +386,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             promote32_percol(acc + (c + 1) * 16, rb, sbs + (c + 1) * 32, sa2);
             if (c + 2 < Cfg::kChunks) tmem_wait_ld(ra);
           }
-          reinterpret_cast<float4*>(sb_mine + ((kb + 1) & 1) * 128)[lane] = sbc_nxt;
+          reinterpret_cast<float4*>(sb_mine + ((i + 1) & 1) * 128)[lane] = sbc_nxt;
           __syncwarp();
         }
         tc_fence_before();
@@ -404,12 +403,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // ---- epilogue: this warp's 32 rows x 128 columns, through TMA stores
       // (addresses are recomputed, not held: the promotion warps have no
       // registers to spare while the accumulators are live)
+      const uint32_t stg = smem_u32(&sm.epi_stage[warp - 4][0]);
       if (w.slot < 0) {
-        store_rows_tma<kOutBf16, kAcc, Cfg::kWarpCols>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_c, col0,
-                                 row - lane);
+        store_rows_tma<kOutBf16, kAcc, Cfg::kWarpCols>(acc, stg, lane, &tmap_c, col0, row - lane);
       } else {
-        store_rows_tma<false, false, Cfg::kWarpCols>(acc, smem_u32(&sm.epi_stage[warp - 4][0]), lane, &tmap_ws, h * Cfg::kWarpCols,
-                              w.slot * kPairTileM + static_cast<int>(rank) * kBM + g * 32);
+        store_rows_tma<false, false, Cfg::kWarpCols>(
+            acc, stg, lane, &tmap_ws, h * Cfg::kWarpCols,
+            w.slot * kPairTileM + static_cast<int>(rank) * kBM + g * 32);
       }
     }
   epilogue_done:
