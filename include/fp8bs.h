@@ -180,7 +180,12 @@ fp8bs_status fp8bs_quant_w_128x128(const void* w, fp8bs_dtype wt, int64_t R, int
  * Requirements: K % 128 == 0; N % 128 == 0 for BLOCK modes, N % 16 == 0 for
  * PERCOL (UNSUPPORTED); A, B, C 16-byte aligned; lda, ldb, ldc*sizeof(ct)
  * multiples of 16 (MISALIGNED); sa, sb 4-byte aligned.  M, N == 0: no-op;
- * K == 0 writes zeros.  Any M >= 1 is allowed (the last row tile is ragged). */
+ * K == 0 writes zeros.  Any M >= 1 is allowed (the last row tile is ragged).
+ * Each output is the FP32 sum over the 128-deep K slabs of (slab partial x sa
+ * x sb); the slab order is fixed per output tile by the shape and the device's
+ * number of SM pairs (forward, or last to first on every other wave of the
+ * persistent walk when a wave's operand panels exceed half of L2), so repeated
+ * calls give identical bits. */
 fp8bs_status fp8bs_gemm(int64_t M, int64_t N, int64_t K,
                         const uint8_t* A, int64_t lda, const float* sa, int64_t ldsa,
                         const uint8_t* B, int64_t ldb, const float* sb, fp8bs_bscale sb_mode,
