@@ -169,6 +169,31 @@ __device__ __forceinline__ void promote32_percol(float2* acc, const uint32_t (&r
   }
 }
 
+// Write box c of this warp's accumulators (32 rows x 64 bytes: FP32 columns
+// 16c .. 16c+15, or BF16 rounded to nearest even, columns 32c .. 32c+31) into
+// 2 KB of shared memory at dst: row `lane` at 64 * lane, its 16-byte unit j at
+// position j ^ ((lane >> 1) & 3) (the 64-byte swizzle of the output maps).
+template <bool kBf16>
+__device__ __forceinline__ void stage_box(const float2* acc, uint32_t dst0, int lane, int c) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {   // 16-byte unit j of this row's 64 bytes
+    const uint32_t dst = dst0 + static_cast<uint32_t>(lane) * 64u +
+                         ((static_cast<uint32_t>(j) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u)) << 4);
+    if constexpr (kBf16) {
+      const int k = c * 16 + 4 * j;   // float2 index of column c*32 + 8j
+      st_shared_v4(dst, make_uint4(pack_bf16x2(acc[k].x, acc[k].y),
+                                   pack_bf16x2(acc[k + 1].x, acc[k + 1].y),
+                                   pack_bf16x2(acc[k + 2].x, acc[k + 2].y),
+                                   pack_bf16x2(acc[k + 3].x, acc[k + 3].y)));
+    } else {
+      // two 8-byte stores straight from the accumulator register pairs
+      const int k = c * 8 + 2 * j;    // float2 index of column c*16 + 4j
+      st_shared_v2f(dst, acc[k]);
+      st_shared_v2f(dst + 8, acc[k + 1]);
+    }
+  }
+}
+
 // Store this warp's 32 rows x kCols accumulator columns (row `lane` per
 // thread) through a 2 KB shared buffer and 64-byte-wide TMA boxes at (col, row)
 // of `tmap`: FP32 (16 columns per box) or BF16 rounded to nearest even (32).
@@ -183,24 +208,7 @@ __device__ __forceinline__ void store_rows_tma(const float2* acc, uint32_t stg, 
     // the previous bulk store of this buffer must have read it
     if (lane == 0) bulk_wait_read_all();
     __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {   // 16-byte unit j of this row's 64 bytes
-      // row `lane` at 64 * lane; 16-byte unit j at position j ^ ((lane >> 1) & 3)
-      const uint32_t dst = stg + static_cast<uint32_t>(lane) * 64u +
-                           ((static_cast<uint32_t>(j) ^ ((static_cast<uint32_t>(lane) >> 1) & 3u)) << 4);
-      if constexpr (kBf16) {
-        const int k = c * 16 + 4 * j;   // float2 index of column c*32 + 8j
-        st_shared_v4(dst, make_uint4(pack_bf16x2(acc[k].x, acc[k].y),
-                                     pack_bf16x2(acc[k + 1].x, acc[k + 1].y),
-                                     pack_bf16x2(acc[k + 2].x, acc[k + 2].y),
-                                     pack_bf16x2(acc[k + 3].x, acc[k + 3].y)));
-      } else {
-        // two 8-byte stores straight from the accumulator register pairs
-        const int k = c * 8 + 2 * j;    // float2 index of column c*16 + 4j
-        st_shared_v2f(dst, acc[k]);
-        st_shared_v2f(dst + 8, acc[k + 1]);
-      }
-    }
+    stage_box<kBf16>(acc, stg, lane, c);
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
@@ -210,6 +218,35 @@ __device__ __forceinline__ void store_rows_tma(const float2* acc, uint32_t stg, 
         tma_store_2d(tmap, col + c * kChunkCols, row, stg);
       bulk_commit_group();
     }
+  }
+}
+
+// Park this warp's 32 rows x kCols accumulator columns in shared memory (one
+// 2 KB box after the other from `park`) and issue their TMA stores as one
+// bulk group without waiting for them: the stores drain while the warp goes on
+// with its next tile.  The previous parked group must have been read before
+// the area is rewritten; the wait at the start covers it (and every earlier
+// store of this thread).
+template <bool kBf16, bool kAdd = false, int kCols = 64>
+__device__ __forceinline__ void park_rows_tma(const float2* acc, uint32_t park, int lane,
+                                              const CUtensorMap* tmap, int col, int row) {
+  constexpr int kChunkCols = kBf16 ? 32 : 16;
+  constexpr int kBoxes = kCols / kChunkCols;
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < kBoxes; ++c) stage_box<kBf16>(acc, park + c * 2048u, lane, c);
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+#pragma unroll
+    for (int c = 0; c < kBoxes; ++c) {
+      if constexpr (kAdd)
+        tma_reduce_add_2d(tmap, col + c * kChunkCols, row, park + c * 2048u);
+      else
+        tma_store_2d(tmap, col + c * kChunkCols, row, park + c * 2048u);
+    }
+    bulk_commit_group();
   }
 }
 

@@ -43,17 +43,33 @@ namespace fp8bs {
 constexpr int kPairTileM = 2 * kBM;             // rows of a pair tile
 constexpr int kPairRingBytes = 6 * 32768;       // operand ring per CTA
 
-template <int BN>
+// kPark: ring stages given up to park half of each warp's finished tile (its
+// TMA stores then drain while the next tile runs).
+template <int BN, int kPark = 0>
 struct PairCfg {
   static_assert(BN == 128 || BN == 256, "pair tile width");
   static constexpr int kStageA = kBM * kBK;              // this CTA's 128 rows of A, one slab
   static constexpr int kStageB = (BN / 2) * kBK;         // this CTA's half of the B tile
   static constexpr int kStageBytes = kStageA + kStageB;
-  static constexpr int kStages = kPairRingBytes / kStageBytes;   // 6 or 8
+  static constexpr int kStages = kPairRingBytes / kStageBytes - kPark;   // 6 or 8, less kPark
   static constexpr int kBufs = kTmemCols / BN;           // TMEM slab buffers: 2 or 4
   static constexpr int kWarpCols = BN / 2;               // columns per promotion warp
   static constexpr int kChunks = kWarpCols / 32;         // x32 TMEM loads per warp and slab
+  // parking area of a promotion warp: its share of the stages given up
+  static constexpr int kParkWarpBytes = kPark * kStageBytes / kEpiWarps;
+  // the last columns of a warp that fit its parking area (32 rows of
+  // kOutBytes-byte outputs), in whole 64-byte boxes
+  template <int kOutBytes>
+  static constexpr int park_cols() {
+    return kParkWarpBytes / (32 * kOutBytes) < kWarpCols ? kParkWarpBytes / (32 * kOutBytes)
+                                                         : kWarpCols;
+  }
 };
+
+// Ring stages each mode gives up for parking: the per-column mode (Wgrad:
+// FP32 output, short K, the largest epilogue per slab) and the block modes.
+constexpr int kPairParkPerCol = 2;
+constexpr int kPairParkBlock = 0;
 // Register split of the pair kernel: its producer warpgroup (TMA and MMA issue
 // loops) keeps 40 per thread so the promotion warpgroups can hold 232
 // (128 x 40 + 256 x 232 = 64512 = 168 x 384).
@@ -182,7 +198,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   extern __shared__ __align__(1024) unsigned char pair_smem_raw[];
   const uint32_t raw_addr = smem_u32(pair_smem_raw);
   unsigned char* ring = pair_smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  using Cfg = PairCfg<BN>;
+  constexpr int kPark = kSb == kSbPerCol ? kPairParkPerCol : kPairParkBlock;
+  using Cfg = PairCfg<BN, kPark>;
   PairSmem<BN>& sm = *reinterpret_cast<PairSmem<BN>*>(ring + static_cast<size_t>(kPairRingBytes));
   const uint32_t ring_addr = smem_u32(ring);
 
@@ -400,12 +417,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         sa_cur = sa_nxt;
         sb_cur = sb_nxt;
       }
-      // ---- epilogue: this warp's 32 rows x 128 columns, through TMA stores
-      // (addresses are recomputed, not held: the promotion warps have no
-      // registers to spare while the accumulators are live)
+      // ---- epilogue: this warp's 32 rows x kWarpCols columns, through TMA
+      // stores (addresses are recomputed, not held: the promotion warps have
+      // no registers to spare while the accumulators are live)
       const uint32_t stg = smem_u32(&sm.epi_stage[warp - 4][0]);
       if (w.slot < 0) {
-        store_rows_tma<kOutBf16, kAcc, Cfg::kWarpCols>(acc, stg, lane, &tmap_c, col0, row - lane);
+        if constexpr (kPark > 0) {
+          // the first columns through the staging buffer, the last kParkCols
+          // parked (their stores drain while the next tile runs)
+          constexpr int kParkCols = Cfg::template park_cols<kOutBf16 ? 2 : 4>();
+          constexpr int kStaged = Cfg::kWarpCols - kParkCols;
+          static_assert(kParkCols % 32 == 0 && kParkCols > 0, "parked columns: whole boxes");
+          if constexpr (kStaged > 0)
+            store_rows_tma<kOutBf16, kAcc, kStaged>(acc, stg, lane, &tmap_c, col0, row - lane);
+          const uint32_t park = ring_addr + Cfg::kStages * Cfg::kStageBytes +
+                                static_cast<uint32_t>(warp - 4) * Cfg::kParkWarpBytes;
+          park_rows_tma<kOutBf16, kAcc, kParkCols>(acc + kStaged / 2, park, lane, &tmap_c,
+                                                   col0 + kStaged, row - lane);
+        } else {
+          store_rows_tma<kOutBf16, kAcc, Cfg::kWarpCols>(acc, stg, lane, &tmap_c, col0,
+                                                         row - lane);
+        }
       } else {
         store_rows_tma<false, false, Cfg::kWarpCols>(
             acc, stg, lane, &tmap_ws, h * Cfg::kWarpCols,
