@@ -70,11 +70,17 @@ struct PairCfg {
 // FP32 output, short K, the largest epilogue per slab) and the block modes.
 constexpr int kPairParkPerCol = 2;
 constexpr int kPairParkBlock = 0;
-// Register split of the pair kernel: its producer warpgroup (TMA and MMA issue
-// loops) keeps 40 per thread so the promotion warpgroups can hold 232
-// (128 x 40 + 256 x 232 = 64512 = 168 x 384).
-constexpr uint32_t kPairProducerRegs = 40;
-constexpr uint32_t kPairEpilogueRegs = 232;
+// Scale ring of the pair kernel: warps 2 and 3 of each CTA load every slab's
+// A and B scales into shared memory ahead of the promotion warps (one entry
+// per operand stage, so both rings advance together), so that no global load
+// latency lies on the promotion's path.
+constexpr int kPairScaleThreads = 64;
+
+// Register split of the pair kernel: its role warpgroup (TMA and MMA issue
+// loops, scale loads) keeps 56 per thread and the promotion warpgroups 224
+// (128 x 56 + 256 x 224 = 64512 = 168 x 384); no spills in either.
+constexpr uint32_t kPairProducerRegs = 56;
+constexpr uint32_t kPairEpilogueRegs = 224;
 static_assert(128 * kPairProducerRegs + 256 * kPairEpilogueRegs <= 168 * kGemmThreads,
               "register split exceeds the launch budget");
 
@@ -85,9 +91,15 @@ struct PairSmem {
   uint64_t done[PairCfg<BN>::kStages];   // both CTAs: the slab's MMAs are complete
   uint64_t tmem_free[PairCfg<BN>::kBufs];  // even CTA: 16 promotion warps released a buffer
   uint64_t drain;
+  uint64_t scl_full[PairCfg<BN>::kStages];   // this CTA: the scale loaders filled an entry
+  uint64_t scl_free[PairCfg<BN>::kStages];   // this CTA: its promotion warps read an entry
   uint32_t tmem_base;
   int32_t abort_flag;
-  alignas(16) float sb_stage[kEpiWarps][2][128];
+  // per slab, in a ring of one entry per operand stage: the A scales of this
+  // CTA's 128 rows, and the B scales of the tile's BN columns (per-column
+  // mode) or of its BN / 128 column blocks (block modes)
+  alignas(16) float scl_sa[PairCfg<BN>::kStages][kBM];
+  alignas(16) float scl_sb[PairCfg<BN>::kStages][BN];
 };
 
 template <int BN>
@@ -218,6 +230,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       mbar_init(&sm.done[s], 1);
     }
     for (int b = 0; b < Cfg::kBufs; ++b) mbar_init(&sm.tmem_free[b], 2 * kEpiWarps);
+    for (int e = 0; e < Cfg::kStages; ++e) {
+      mbar_init(&sm.scl_full[e], kPairScaleThreads);
+      mbar_init(&sm.scl_free[e], kEpiWarps);
+    }
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbarrier_init();
@@ -316,61 +332,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         mma_commit_pair(&sm.drain, 0x1);
         bounded_wait_noabort(&sm.drain, 0, kSpinLimitNs);
       }
+    } else if (warp >= 2) {
+      // ------------------------------------------------------------ scales
+      // Every slab's scales into the next free ring entry with asynchronous
+      // copies that arrive on the entry's barrier when they land, so that the
+      // loads of several slabs are in flight at once: thread lt copies the A
+      // scales of rows lt and 64 + lt, and 4 B scales (per-column mode) or one
+      // column block's scale (block modes, BN / 128 threads).  Rows past M and
+      // columns past N get zeros.
+      const int lt = static_cast<int>(threadIdx.x) - 64;
+      int e = 0;
+      uint32_t ephase = 0;
+      for (int u = PAIR_FIRST; u < p.units; u += PAIR_STRIDE) {
+        const PairUnit w = pair_unit(u, p);
+        int mt, nt;
+        pair_tile_mn(w.tile, p, mt, nt);
+        const int row0 = mt * kPairTileM + static_cast<int>(rank) * kBM;
+        const int n0 = nt * BN;
+        // block modes: this thread's column block (threads 0 .. BN/128 - 1)
+        const int cb = n0 / 128 + (lt < BN / 128 ? lt : 0);
+        const bool cb_ok = cb * 128 < p.N;
+        const float* sb_k = p.sb + static_cast<int64_t>(cb_ok ? cb : 0) * p.sb_n_stride;
+        const uint32_t cb_bytes = cb_ok ? 4u : 0u;
+        for (int i = w.kb0; i < w.kb1; ++i) {
+          const int kb = pair_kb(w, i);
+          if (!bounded_wait(&sm.scl_free[e], ephase ^ 1u, abort_flag)) goto scales_done;
+          const float* sa_k = p.sa + static_cast<int64_t>(kb) * p.ldsa;
+#pragma unroll
+          for (int r = lt; r < kBM; r += kPairScaleThreads) {
+            const bool ok = row0 + r < p.M;
+            cp_async_4(smem_u32(&sm.scl_sa[e][r]), sa_k + (ok ? row0 + r : 0), ok ? 4u : 0u);
+          }
+          if constexpr (kSb == kSbPerCol) {
+#pragma unroll
+            for (int j = lt * 4; j < BN; j += 4 * kPairScaleThreads) {
+              // N is a multiple of 16: columns n0+j .. n0+j+3 are all in or all out
+              const bool ok = n0 + j < p.N;
+              cp_async_16(smem_u32(&sm.scl_sb[e][j]),
+                          p.sb + static_cast<int64_t>(kb) * p.ldsb + (ok ? n0 + j : 0),
+                          ok ? 16u : 0u);
+            }
+          } else {
+            if (lt < BN / 128)
+              cp_async_4(smem_u32(&sm.scl_sb[e][lt]), sb_k + static_cast<int64_t>(kb) * p.sb_k_stride,
+                         cb_bytes);
+          }
+          cp_async_arrive(&sm.scl_full[e]);
+          if (++e == Cfg::kStages) {
+            e = 0;
+            ephase ^= 1u;
+          }
+        }
+      }
+    scales_done:
+      cp_async_wait_all();   // this thread's copies have landed before the CTA may exit
     }
   } else {
     regs_alloc<kPairEpilogueRegs>();
     // ------------------------------------------------- promotion + epilogue
     const int g = warp & 3;          // TMEM lane group (rows 32g .. 32g+31 of this CTA)
     const int h = (warp - 4) >> 2;   // column half of the tile (kWarpCols columns each)
-    int buf = 0, stage = 0;
+    int buf = 0, stage = 0;   // the slab's TMEM buffer; its operand stage and scale entry
     uint32_t phase = 0;
     for (int u = PAIR_FIRST; u < p.units; u += PAIR_STRIDE) {
       const PairUnit w = pair_unit(u, p);
       int mt, nt;
       pair_tile_mn(w.tile, p, mt, nt);
       const int row = mt * kPairTileM + static_cast<int>(rank) * kBM + g * 32 + lane;
-      const bool row_ok = row < p.M;
       const int col0 = nt * BN + h * Cfg::kWarpCols;
-      const bool cols_ok = col0 < p.N;
       float2 acc[Cfg::kWarpCols / 2];
 #pragma unroll
       for (int i = 0; i < Cfg::kWarpCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
-      // slab kb's scales; 0 for a slab outside [0, KB) (the one after a unit's last)
-      auto in_k = [&](int kb) { return static_cast<unsigned>(kb) < static_cast<unsigned>(p.KB); };
-      auto load_sa = [&](int kb) -> float {
-        return (row_ok && in_k(kb)) ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ldsa + row) : 0.0f;
-      };
-      // block mode: this warp's column block of B scales (one pointer kept)
-      const float* sb_blk = p.sb + static_cast<int64_t>(col0 / 128) * p.sb_n_stride;
-      auto load_sb = [&](int kb) -> float {
-        if constexpr (kSb == kSbBlock) {
-          return (cols_ok && in_k(kb)) ? __ldg(sb_blk + static_cast<int64_t>(kb) * p.sb_k_stride)
-                                       : 0.0f;
-        } else {
-          return 0.0f;
-        }
-      };
-      const int kfirst = pair_kb(w, w.kb0);
-      float sa_cur = load_sa(kfirst), sb_cur = load_sb(kfirst);
-      // per-column mode: this warp's 128 B scales of a slab, staged in smem
-      float* sb_mine = &sm.sb_stage[warp - 4][0][0];
-      auto fetch_sb_cols = [&](int kb) -> float4 {
-        const int c = col0 + lane * 4;
-        return (in_k(kb) && c < p.N)
-                   ? __ldg(reinterpret_cast<const float4*>(p.sb + static_cast<int64_t>(kb) * p.ldsb + c))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      };
-      if constexpr (kSb == kSbPerCol) {
-        const float4 v = fetch_sb_cols(kfirst);
-        reinterpret_cast<float4*>(sb_mine + (w.kb0 & 1) * 128)[lane] = v;
-        __syncwarp();
-      }
       for (int i = w.kb0; i < w.kb1; ++i) {
-        const int kb_nxt = pair_kb(w, i + 1);
-        const float sa_nxt = load_sa(kb_nxt), sb_nxt = load_sb(kb_nxt);
-        float4 sbc_nxt;
-        if constexpr (kSb == kSbPerCol) sbc_nxt = fetch_sb_cols(kb_nxt);
+        // the slab's scales, loaded ahead into the ring by warps 2 and 3 (rows
+        // past M and columns past N carry zero scales, so no guard is needed)
+        if (!bounded_wait(&sm.scl_full[stage], phase, abort_flag)) goto epilogue_done;
+        const float sa = sm.scl_sa[stage][g * 32 + lane];
+        float sb = 0.0f;
+        if constexpr (kSb == kSbBlock) sb = sm.scl_sb[stage][(h * Cfg::kWarpCols) / 128];
         if (!bounded_wait(&sm.done[stage], phase, abort_flag)) goto epilogue_done;
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) +
@@ -379,7 +419,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tmem_ld32(taddr, ra);
         tmem_wait_ld(ra);
         if constexpr (kSb == kSbBlock) {
-          const float sc = sa_cur * sb_cur;
+          const float sc = sa * sb;
           const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
           for (int c = 0; c < Cfg::kChunks; c += 2) {
@@ -391,9 +431,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             if (c + 2 < Cfg::kChunks) tmem_wait_ld(ra);
           }
         } else {
-          // columns past N carry zero scales (and zero products), so no guard is needed
-          const float2 sa2 = make_float2(sa_cur, sa_cur);
-          const float* sbs = sb_mine + (i & 1) * 128;   // staged by step, not by slab
+          const float2 sa2 = make_float2(sa, sa);
+          const float* sbs = &sm.scl_sb[stage][h * Cfg::kWarpCols];
 #pragma unroll
           for (int c = 0; c < Cfg::kChunks; c += 2) {
             tmem_ld32(taddr + (c + 1) * 32, rb);
@@ -403,19 +442,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             promote32_percol(acc + (c + 1) * 16, rb, sbs + (c + 1) * 32, sa2);
             if (c + 2 < Cfg::kChunks) tmem_wait_ld(ra);
           }
-          reinterpret_cast<float4*>(sb_mine + ((i + 1) & 1) * 128)[lane] = sbc_nxt;
-          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.tmem_free[buf]), 0));
+        if (lane == 0) {
+          mbar_arrive_cluster(mapa_shared(smem_u32(&sm.tmem_free[buf]), 0));
+          mbar_arrive(&sm.scl_free[stage]);
+        }
         if (++buf == Cfg::kBufs) buf = 0;
         if (++stage == Cfg::kStages) {
           stage = 0;
           phase ^= 1u;
         }
-        sa_cur = sa_nxt;
-        sb_cur = sb_nxt;
       }
       // ---- epilogue: this warp's 32 rows x kWarpCols columns, through TMA
       // stores (addresses are recomputed, not held: the promotion warps have
