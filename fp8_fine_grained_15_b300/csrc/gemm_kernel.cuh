@@ -58,6 +58,7 @@ constexpr int kMaxExperts = 1024;
 
 enum SbKind : int { kSbBlock = 0, kSbPerCol = 1 };
 constexpr int kEpiStageBytes = 32 * 64;   // one warp's output chunk: 32 rows x 64 B
+constexpr int kScaleThreads = 64;         // warps 2 and 3: the scale loaders
 
 struct GemmParams {
   int32_t M;            // rows of A / C (M_cap for the grouped call)
@@ -110,9 +111,13 @@ struct GemmSmem {
   // grouped: first tile index of each expert; expert e owns tiles
   // tile_base[e] .. tile_base[e+1]-1, its m tiles fastest, then its n tiles
   int32_t tile_base[kMaxExperts + 1];
-  // per-column B scales of the current and the next slab, one copy per
-  // promotion warp (its 128 columns)
-  alignas(16) float sb_stage[kEpiWarps][2][128];
+  // scale ring, one entry per operand stage: warps 2 and 3 copy each slab's
+  // A scales (the tile's 128 rows) and B scales (its 256 columns, per-column
+  // mode, or its two column blocks, block mode) ahead of the promotion warps
+  uint64_t scl_full[kStages];   // the copies of an entry have landed (64 arrivals)
+  uint64_t scl_free[kStages];   // the promotion warps read it (kEpiWarps arrivals)
+  alignas(16) float scl_sa[kStages][kBM];
+  alignas(16) float scl_sb[kStages][kBN];
 };
 
 constexpr size_t kGemmSmemBytes =
@@ -276,6 +281,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&sm.tfull[b], 1);
       mbar_init(&sm.tempty[b], kEpiWarps);
     }
+    for (int e = 0; e < kStages; ++e) {
+      mbar_init(&sm.scl_full[e], kScaleThreads);
+      mbar_init(&sm.scl_free[e], kEpiWarps);
+    }
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     sm.bad_offsets = 0;
@@ -401,6 +410,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mma_commit(&sm.drain);
       bounded_wait_noabort(&sm.drain, 0, kSpinLimitNs);
     }
+  } else if (!skip_all && warp >= 2) {
+    // ---------------------------------------------------------------- scales
+    // Every slab's scales into the next free ring entry with asynchronous
+    // copies that arrive on the entry's barrier when they land: thread lt
+    // copies the A scales of rows lt and 64 + lt, and 4 B scales (per-column
+    // mode) or one column block's scale (block mode, threads 0 and 1).  Rows
+    // past M and columns past N get zeros.
+    const int lt = static_cast<int>(threadIdx.x) - 64;
+    int e = 0;
+    uint32_t ephase = 0;
+    for (int t = blockIdx.x; t < FP8BS_NUM_TILES; t += gridDim.x) {
+      const TileCoord tc = tile_coord(t, p, sm);
+      const float* sbe = p.sb + static_cast<int64_t>(tc.e) * p.sb_e_stride;
+      const int cb = tc.n0 / 128 + (lt < kBN / 128 ? lt : 0);
+      const bool cb_ok = cb * 128 < p.N;
+      const float* sb_k = sbe + static_cast<int64_t>(cb_ok ? cb : 0) * p.sb_n_stride;
+      for (int kb = 0; kb < p.KB; ++kb) {
+        if (!bounded_wait(&sm.scl_free[e], ephase ^ 1u, abort_flag)) goto scales_done;
+        const float* sa_k = p.sa + static_cast<int64_t>(kb) * p.ldsa;
+#pragma unroll
+        for (int r = lt; r < kBM; r += kScaleThreads) {
+          const bool ok = tc.m0 + r < p.M;
+          cp_async_4(smem_u32(&sm.scl_sa[e][r]), sa_k + (ok ? tc.m0 + r : 0), ok ? 4u : 0u);
+        }
+        if constexpr (kSb == kSbPerCol) {
+#pragma unroll
+          for (int j = lt * 4; j < kBN; j += 4 * kScaleThreads) {
+            // N is a multiple of 16: columns n0+j .. n0+j+3 are all in or all out
+            const bool ok = tc.n0 + j < p.N;
+            cp_async_16(smem_u32(&sm.scl_sb[e][j]),
+                        sbe + static_cast<int64_t>(kb) * p.ldsb + (ok ? tc.n0 + j : 0),
+                        ok ? 16u : 0u);
+          }
+        } else {
+          if (lt < kBN / 128)
+            cp_async_4(smem_u32(&sm.scl_sb[e][lt]), sb_k + static_cast<int64_t>(kb) * p.sb_k_stride,
+                       cb_ok ? 4u : 0u);
+        }
+        cp_async_arrive(&sm.scl_full[e]);
+        if (++e == kStages) {
+          e = 0;
+          ephase ^= 1u;
+        }
+      }
+    }
+  scales_done:
+    cp_async_wait_all();   // this thread's copies have landed before the CTA may exit
   }
   } else {
     regs_alloc<kEpilogueRegs>();
@@ -410,50 +466,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int h = (warp - 4) >> 2;   // column half (0: 0..127, 1: 128..255)
     int buf = 0;
     uint32_t tphase = 0;
+    // scale ring position: entry sk % kStages, parity sk / kStages
+    static_assert((kStages & (kStages - 1)) == 0, "ring position arithmetic");
+    uint32_t sk = 0;
     for (int t = blockIdx.x; t < FP8BS_NUM_TILES; t += gridDim.x) {
       const TileCoord tc = tile_coord(t, p, sm);
-      const int row = tc.m0 + g * 32 + lane;
-      const bool row_ok = row < p.M;
       const int col0 = tc.n0 + h * 128;
-      const bool cols_ok = col0 < p.N;
-      const float* sbe = p.sb + static_cast<int64_t>(tc.e) * p.sb_e_stride;
       float2 acc[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
-      auto load_sa = [&](int kb) -> float {
-        return (row_ok && kb < p.KB) ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ldsa + row)
-                                     : 0.0f;
-      };
-      auto load_sb = [&](int kb) -> float {
-        if constexpr (kSb == kSbBlock) {
-          return (cols_ok && kb < p.KB)
-                     ? __ldg(sbe + static_cast<int64_t>(kb) * p.sb_k_stride +
-                             static_cast<int64_t>(col0 / 128) * p.sb_n_stride)
-                     : 0.0f;
-        } else {
-          return 0.0f;
-        }
-      };
-      float sa_cur = load_sa(0), sb_cur = load_sb(0);
-      // per-column mode: this warp's 128 B scales of a slab, staged in smem
-      float* sb_mine = &sm.sb_stage[warp - 4][0][0];
-      auto fetch_sb_cols = [&](int kb) -> float4 {
-        const int c = col0 + lane * 4;
-        return (kb < p.KB && c < p.N)
-                   ? __ldg(reinterpret_cast<const float4*>(sbe + static_cast<int64_t>(kb) * p.ldsb + c))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      };
-      if constexpr (kSb == kSbPerCol) {
-        const float4 v = fetch_sb_cols(0);
-        reinterpret_cast<float4*>(sb_mine)[lane] = v;
-        __syncwarp();
-      }
       for (int kb = 0; kb < p.KB; ++kb) {
-        const float sa_nxt = load_sa(kb + 1), sb_nxt = load_sb(kb + 1);
-        float4 sbc_nxt;
-        if constexpr (kSb == kSbPerCol) sbc_nxt = fetch_sb_cols(kb + 1);
+        // the slab's scales, copied ahead into the ring by warps 2 and 3 (rows
+        // past M and columns past N carry zero scales, so no guard is needed)
+        const uint32_t se = sk & (kStages - 1);
         if (!bounded_wait(&sm.tfull[buf], tphase, abort_flag)) goto epilogue_done;
+        if (!bounded_wait(&sm.scl_full[se], sk / kStages, abort_flag)) goto epilogue_done;
+        const float sa = sm.scl_sa[se][g * 32 + lane];
+        float sb = 0.0f;
+        if constexpr (kSb == kSbBlock) sb = sm.scl_sb[se][h];
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(g * 32) << 16) +
                                static_cast<uint32_t>(buf * kBN + h * 128);
@@ -461,7 +492,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tmem_ld32(taddr, ra);
         tmem_wait_ld(ra);
         if constexpr (kSb == kSbBlock) {
-          const float sc = sa_cur * sb_cur;
+          const float sc = sa * sb;
           const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
           for (int c = 0; c < 4; c += 2) {
@@ -473,9 +504,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (c + 2 < 4) tmem_wait_ld(ra);
           }
         } else {
-          // columns past N carry zero scales (and zero products), so no guard is needed
-          const float2 sa2 = make_float2(sa_cur, sa_cur);
-          const float* sbs = sb_mine + (kb & 1) * 128;
+          const float2 sa2 = make_float2(sa, sa);
+          const float* sbs = &sm.scl_sb[se][h * 128];
 #pragma unroll
           for (int c = 0; c < 4; c += 2) {
             tmem_ld32(taddr + (c + 1) * 32, rb);
@@ -485,18 +515,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             promote32_percol(acc + (c + 1) * 16, rb, sbs + (c + 1) * 32, sa2);
             if (c + 2 < 4) tmem_wait_ld(ra);
           }
-          reinterpret_cast<float4*>(sb_mine + ((kb + 1) & 1) * 128)[lane] = sbc_nxt;
-          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.tempty[buf]);
+        if (lane == 0) {
+          mbar_arrive(&sm.tempty[buf]);
+          mbar_arrive(&sm.scl_free[se]);
+        }
         if (++buf == 2) {
           buf = 0;
           tphase ^= 1u;
         }
-        sa_cur = sa_nxt;
-        sb_cur = sb_nxt;
+        sk = (sk + 1) & (2 * kStages - 1);
       }
       // ---- epilogue: this warp's 32 rows x 128 columns, through TMA stores
       // (rows of a tile never straddle two experts: expert ranges are whole tiles)
