@@ -20,7 +20,9 @@
 //   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32)
 //               per slab into one of two TMEM slab buffers (256 columns each);
 //               commits release the smem stage and publish the slab.
-//   warps 2,3   idle (they complete the producer warpgroup)
+//   warps 2,3   scale loaders: every slab's A and B scales into a shared-memory
+//               ring (one entry per operand stage) with cp.async, ahead of
+//               the promotion warps
 //   warps 4..11 promotion + epilogue: tcgen05.ld the slab (32 rows x 128
 //               columns per warp), acc += P * (sa[row] * sb) in FP32 registers
 //               (packed f32x2 FMAs), release the TMEM buffer; after the last

@@ -13,8 +13,9 @@
 // cluster of two CTAs computes a 256 x BN tile with one pair MMA: each CTA
 // stages its own 128 rows of A and one half (BN/2 rows) of B.
 //
-// Tile width BN: 256 (32 KB per SM and slab, 6 stages, two 256-column TMEM
-// slab buffers) is what the library launches.  BN = 128 (24 KB, 8 stages, four
+// Tile width BN: 256 (32 KB per SM and slab, 6 stages -- 4 in the per-column
+// mode, which parks output in the other two -- and two 256-column TMEM slab
+// buffers) is what the library launches.  BN = 128 (24 KB, 8 stages, four
 // 128-column buffers) compiles and passes the parity tests; pair MMAs with
 // N = 128 stream at 97 % of the N = 256 rate in isolation, but with 45 % more
 // operand bytes per FLOP the whole kernel measured 1.4-2x slower on the
@@ -27,12 +28,19 @@
 //               N=256, K=32) per slab into one of two 256-column TMEM buffers,
 //               then one commit that arrives on `done[stage]` in both CTAs:
 //               the stage may be refilled and the TMEM slab may be read.
+//   warps 2, 3  scale loaders: every slab's A scales (this CTA's 128 rows)
+//               and B scales (the tile's columns or column blocks) into a
+//               shared-memory ring, one entry per operand stage, with cp.async
+//               that arrives on the entry's `scl_full` barrier.
 //   warps 4..11 promotion + epilogue of this CTA's 128 rows (as in the
 //               single-CTA kernel); each warp releases its TMEM columns by
-//               arriving on the even CTA's `tmem_free` barrier (16 arrivals).
+//               arriving on the even CTA's `tmem_free` barrier (16 arrivals)
+//               and its scale entry on `scl_free`.
 //               The epilogue goes out through TMA stores: each warp writes a
 //               32-row x 64-byte chunk of its rows into a 2 KB shared buffer
-//               (64-byte swizzle, conflict-free) and one lane stores the box.
+//               (64-byte swizzle, conflict-free) and one lane stores the box;
+//               in the per-column mode half of the tile is parked in two
+//               ring stages given up for it and drains during the next tile.
 //               (Stores straight from registers, one row per lane, hit 32
 //               cache lines per instruction: ~13k cycles per FP32 tile.)
 #pragma once
