@@ -518,7 +518,7 @@ def run_extras(dev, stream, peaks):
 
 # Bounded samples of the layer step for the oracle: the full K and N, fewer
 # tokens (the work per token is the same, so the rate carries over).
-CPU_BASELINE_TOKENS = 512     # one run inside the fp8bs arm: ~10-20 s on 16 cores
+CPU_BASELINE_TOKENS = 1024    # one run inside the fp8bs arm: ~16 s on 16 cores
 REFERENCE_STEP_TOKENS = 256   # one step of the reference arm
 
 
