@@ -243,6 +243,11 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 
 // L2 policy for operand tiles read only by the CTAs of one wave (the B panels
 // of the m-fastest walk): let them go first.
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
