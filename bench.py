@@ -87,7 +87,7 @@ def dual_bytes(elems: int, in_bytes: int) -> float:
 NCU_TRAFFIC = {
     # one launch of `bench.py --case wgrad`, measured by ncu on that launch
     "gemm_wgrad": {"files": ("gemm_pair_kernel.cuh", "gemm_kernel.cuh", "ptx.cuh"),
-                   "src": "47c133d1dea9816e", "bytes": 232242176 + 496796416},
+                   "src": "93c8807ed3244986", "bytes": 156778752 + 499927808},
 }
 
 
