@@ -87,7 +87,7 @@ def dual_bytes(elems: int, in_bytes: int) -> float:
 NCU_TRAFFIC = {
     # one launch of `bench.py --case wgrad`, measured by ncu on that launch
     "gemm_wgrad": {"files": ("gemm_pair_kernel.cuh", "gemm_kernel.cuh", "ptx.cuh"),
-                   "src": "93c8807ed3244986", "bytes": 156778752 + 499927808},
+                   "src": "b1df381dda21827f", "bytes": 156778752 + 499927808},
 }
 
 
