@@ -277,10 +277,11 @@ struct SplitPlan {
 };
 constexpr int kMaxSplits = 32;
 // m tiles per group of the pair GEMM's tile walk (see pair_tile_mn), measured on
-// the layer's GEMMs: 8 for the block-scale modes (Dgrad 0.528 -> 0.438 ms,
-// Fprop 0.434 -> 0.410 ms against one group of all m tiles; 4 and 16 slower);
-// the per-column mode (Wgrad, K = tokens: panels of 1 MB stay in L2 anyway)
-// walks m tiles fastest over all of M (0.6205 -> 0.610 ms).
+// the layer's GEMMs: one group of all m tiles when the whole of A fits in a
+// quarter of L2 (its panels then stay there from wave to wave and every B
+// panel is read once: Fprop, A = 29 MB, 0.385 -> 0.380 ms against groups of 8;
+// Wgrad, A = 29 MB, 0.6205 -> 0.610 ms), else groups of 8 (Dgrad, A = 75 MB:
+// 0.528 -> 0.438 ms against one group; 4, 6, 12 and 16 slower).
 constexpr int kPairGroupM = 8;
 
 // Tile width of the pair GEMM.  256 for every mode: measured on the layer's
@@ -459,12 +460,12 @@ fp8bs_status gemm_dense(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
   p.C = C;
   p.ldc = ldc;
   p.offsets = nullptr;
-  p.group_m = (sb_mode == FP8BS_SB_PERCOL || p.num_m_tiles < kPairGroupM) ? p.num_m_tiles
-                                                                           : kPairGroupM;
   int clusters = 0;
   if ((st = pair_cluster_count(&clusters)) != FP8BS_OK) return st;
   DeviceInfo di;
   if ((st = device_info(&di)) != FP8BS_OK) return st;
+  p.group_m = (p.num_m_tiles < kPairGroupM || M * K <= di.l2_bytes / 4) ? p.num_m_tiles
+                                                                       : kPairGroupM;
   {
     // operand panels a wave of clusters reads: its group's A panels and the
     // B panels of its n tiles, each 256 rows x K bytes
